@@ -1,0 +1,170 @@
+/*
+ * stt.h -- C ABI of the EAGLE-3 training-time-test (TTT) draft-step core on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, as defined by the xllm-io review of "SpecForge: A Flexible
+ * and Efficient Open-Source Training Framework for Speculative Decoding"
+ * (cited as "SpecForge review"):
+ *
+ *  1. Sparse-tree TTT attention (SpecForge review, §三 "稀疏树注意力" and §四
+ *     "BlockMask 构造").  At TTT step k the queries q attend to the
+ *     concatenation of k+1 KV blocks (each Q_LEN rows) under the mask
+ *         M = (q >= kv AND kv < T) OR
+ *             (kv >= Q_LEN AND kv mod Q_LEN < T AND (kv - q) mod Q_LEN == 0)
+ *     i.e. block 0 is causal with the padded columns kv >= T cut, and a query
+ *     q < T additionally sees exactly key q of every later block j = 1..k.
+ *     Queries q >= T ("padded rows") see the T keys kv < T and nothing else.
+ *
+ *  2. Masked soft-target softmax cross-entropy with the gradient written in
+ *     place over the logits (SpecForge review, §三 "内存高效梯度计算", §四
+ *     "掩码 Softmax 损失" / "原地反向传播"):
+ *         pi = softmax(z_r), l_r = -sum_v p_rv log pi_rv,
+ *         s_r = sum_v p_rv g_r,  z_rv <- -(p_rv g_r - pi_rv s_r),
+ *         L = sum_r g_r l_r.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers into memory the caller owns
+ *    (cudaMalloc'd, or a framework's allocator); arrays of pointers and T are
+ *    HOST arrays.  The library allocates no device memory, never synchronises
+ *    the device, and enqueues all work on `stream` (a cudaStream_t passed as
+ *    void*; NULL means the legacy default stream).
+ *  - Argument errors are detected on the host before any launch and returned
+ *    as a negative stt_status; nothing is enqueued in that case.  A CUDA
+ *    launch error is returned as STT_ERR_CUDA.  No C++ exception crosses the
+ *    ABI.  Functions are thread-safe; calls that share output buffers must be
+ *    ordered by the caller.
+ *  - Asynchronous device-side failures (a bounded wait that ran out inside a
+ *    kernel) are recorded in a library-wide error word that
+ *    stt_device_error() reads and clears.
+ *  - Layouts are dense row-major (C order), innermost dimension last.
+ */
+#ifndef STT_H_
+#define STT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define STT_API __attribute__((visibility("default")))
+#else
+#define STT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  STT_OK = 0,
+  STT_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad T, H % H_kv != 0 ... */
+  STT_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. D not 64/128)  */
+  STT_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned               */
+  STT_ERR_CUDA = -4,        /* a CUDA call failed (launch or driver)          */
+  STT_ERR_TIMEOUT = -5,     /* a kernel's bounded wait ran out (device word)  */
+  STT_ERR_WORKSPACE = -6    /* workspace missing or smaller than required     */
+} stt_status;
+
+/* Limits of this build. */
+#define STT_MAX_BATCH 1024   /* B: T[] travels in the kernel parameters */
+#define STT_MAX_STEP 31      /* k: at most 32 KV blocks                 */
+
+/* Static, NUL-terminated description of a status code.  Thread-safe. */
+STT_API const char* stt_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+STT_API int stt_version(void);
+
+/*
+ * Reads and clears the device-side error word (bitwise OR of the STT_DEVERR_*
+ * sites whose bounded wait ran out since the last call).  Synchronises
+ * `stream` first.  Returns STT_OK and stores the word in *word, or
+ * STT_ERR_CUDA.
+ */
+STT_API int stt_device_error(void* stream, uint32_t* word);
+
+/* --------------------------------------------------------------------------
+ * Sparse-tree attention, forward.
+ *
+ *  q        bf16 [B, H, Q_LEN, D], the step-k queries.
+ *  k_blocks host array of k+1 device pointers; k_blocks[j] is bf16
+ *           [B, H_kv, Q_LEN, D], the keys of TTT block j (block 0 = causal).
+ *  v_blocks host array of k+1 device pointers, same shape as k_blocks[j].
+ *  T_host   host int32 [B], valid length of each sequence, 0 <= T[b] <= Q_LEN.
+ *  B        1 <= B <= STT_MAX_BATCH.
+ *  H, H_kv  query / KV heads; H % H_kv == 0; query head h reads KV head
+ *           h / (H / H_kv).
+ *  D        head dimension, 64 or 128.
+ *  Q_LEN    block length, >= 1.
+ *  k        TTT step, 0 <= k <= STT_MAX_STEP.
+ *  scale    softmax scale applied to q.K (1/sqrt(D) in the usual case).
+ *  out      bf16 [B, H, Q_LEN, D]: O = softmax(scale q Kc^T + mask) Vc,
+ *           rounded to nearest even.  A row with no visible key (T[b] = 0)
+ *           is written as zeros.
+ *  lse      fp32 [B, H, Q_LEN]: natural-log logsumexp of the visible scaled
+ *           scores (-inf for a row with no visible key).
+ *  All device pointers must be 16-byte aligned (TMA requirement).
+ * ------------------------------------------------------------------------ */
+STT_API int stt_attn_fwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                 float scale, void* out, float* lse, void* stream);
+
+/* Bytes of device workspace stt_attn_bwd needs for these sizes (>= 16). */
+STT_API size_t stt_attn_bwd_workspace_size(int B, int H, int H_kv, int D, int Q_LEN, int k);
+
+/* --------------------------------------------------------------------------
+ * Sparse-tree attention, backward: the gradient of sum(O * dout) with respect
+ * to q and every K/V block (the page trains through this attention; the
+ * backward is the derivative of the definition, recomputing P from lse).
+ *
+ *  q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale: as forward.
+ *  out      bf16 [B, H, Q_LEN, D], the forward output.
+ *  dout     bf16 [B, H, Q_LEN, D], upstream gradient of out.
+ *  lse      fp32 [B, H, Q_LEN], the forward logsumexp.
+ *  dq       fp32 [B, H, Q_LEN, D], OVERWRITTEN with dL/dq.
+ *  dk_blocks host array of k+1 device pointers, fp32 [B, H_kv, Q_LEN, D],
+ *           each OVERWRITTEN with dL/dK_j (summed over the query heads of the
+ *           group; zero for rows no query sees).
+ *  dv_blocks same for dL/dV_j.
+ *  workspace device scratch of at least stt_attn_bwd_workspace_size() bytes,
+ *           16-byte aligned; contents on entry are ignored.
+ * ------------------------------------------------------------------------ */
+STT_API int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                 float scale, const void* out, const void* dout, const float* lse, float* dq,
+                 float* const* dk_blocks, float* const* dv_blocks, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace soft_ce_fwd_bwd_inplace needs (>= 16). */
+STT_API size_t soft_ce_workspace_size(int64_t N, int64_t V);
+
+/* --------------------------------------------------------------------------
+ * Masked soft-target cross-entropy, loss and in-place gradient, one pass.
+ *
+ *  z        fp32 [N, V] logits; OVERWRITTEN with dL/dz = pi*s - p*g.
+ *  p        fp32 [N, V] target distribution (rows need not sum to 1).
+ *  g        fp32 [N] per-row upstream gradient / loss weight (mask / N).
+ *  N        rows, >= 0.   V  vocabulary, >= 1.
+ *  row_loss fp32 [N] or NULL: l_r = -sum_v p log softmax(z_r) for rows with
+ *           g_r != 0, and 0 for rows with g_r == 0 (masked rows are not read).
+ *  loss     fp32 scalar (device): L = sum_r g_r l_r, summed in a fixed order
+ *           (deterministic).  0 when N == 0.
+ *  workspace device scratch of at least soft_ce_workspace_size(N, V) bytes.
+ *  Rows with g_r == 0 get an exact-zero gradient.  z and p should be 16-byte
+ *  aligned with V % 4 == 0 for the bulk-copy path; other layouts take a
+ *  slower element-wise path with identical results.
+ * ------------------------------------------------------------------------ */
+STT_API int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, int64_t N, int64_t V,
+                            float* row_loss, float* loss, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Device error-word bits (sites of bounded waits). */
+#define STT_DEVERR_FWD_WAIT 0x1u
+#define STT_DEVERR_BWD_WAIT 0x2u
+#define STT_DEVERR_CE_WAIT 0x4u
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STT_H_ */

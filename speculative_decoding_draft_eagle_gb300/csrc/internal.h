@@ -1,0 +1,58 @@
+// internal.h -- declarations shared by the host-side ABI (stt_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace stt {
+
+// ------------------------------------------------------------- soft-CE ----
+struct CePlan {
+  bool bulk;     // bulk-copy (TMA) path: 16-byte aligned rows
+  int C;         // CTAs per row (thread-block cluster size)
+  int slice;     // elements of a row per CTA
+  int smem;      // dynamic shared memory bytes per CTA
+};
+CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V);
+constexpr int64_t kCeMaxV = 409600;  // 16 CTAs x 25600 elements
+cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const float* g, int64_t N,
+                           int64_t V, float* row_loss, float* loss, float* wl, cudaStream_t s);
+
+// ----------------------------------------------------------- attention ----
+constexpr int kMaxBatch = 1024;
+constexpr int kMaxBlocks = 32;
+
+struct AttnArgs {
+  const void* q;
+  const void* k_blocks[kMaxBlocks];
+  const void* v_blocks[kMaxBlocks];
+  int B, H, H_kv, D, Q_LEN, k;
+  float scale;
+  int T[kMaxBatch];
+};
+
+cudaError_t attn_fwd_launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s);
+
+struct AttnBwdArgs {
+  const void* out;
+  const void* dout;
+  const float* lse;
+  float* dq;
+  float* dk_blocks[kMaxBlocks];
+  float* dv_blocks[kMaxBlocks];
+  float* delta;  // workspace: [B, H, Q_LEN] fp32
+};
+size_t attn_bwd_workspace(int B, int H, int Q_LEN);
+cudaError_t attn_bwd_launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s);
+
+// Per-file device error words (read and cleared).
+cudaError_t soft_ce_error_word(uint32_t* w);
+cudaError_t attn_fwd_error_word(uint32_t* w);
+cudaError_t attn_bwd_error_word(uint32_t* w);
+
+// Resolves cuTensorMapEncodeTiled through the runtime (no link against libcuda).
+void* tensor_map_encoder();
+
+}  // namespace stt

@@ -1,0 +1,322 @@
+// soft_ce.cu -- masked soft-target softmax cross-entropy with the gradient
+// written in place over the logits (SpecForge review, §三 "内存高效梯度计算",
+// §四 "掩码 Softmax 损失" / "原地反向传播").
+//
+// Per row r:  m = max z, l = sum exp(z - m), lse = m + log l,
+//             Sp = sum p, Spz = sum p z, loss_r = lse Sp - Spz,
+//             s = g_r Sp, z <- exp(z - lse) s - p g_r.
+//
+// Design (HBM-bound: 12 bytes per element, read z, read p, write z):
+//   * One row is split across a thread-block cluster of C CTAs; each CTA pulls
+//     its slice of z and p into shared memory with bulk (TMA) copies, so every
+//     byte of z and p is read from HBM exactly once.
+//   * Each CTA reduces its slice to (max, sum exp, Sp, Spz); the C partials are
+//     exchanged through distributed shared memory and combined with the usual
+//     max-rescaling, so every CTA knows the row's lse.
+//   * The gradient is computed from the shared-memory copy and streamed out with
+//     coalesced 16-byte stores.  Rows with g = 0 are never read: their gradient
+//     is exactly zero and is written directly.
+//   * Per-row weighted losses g_r * loss_r go to the workspace; a one-CTA kernel
+//     sums them in a fixed order, so the scalar loss is deterministic.
+#include <cmath>
+
+#include "../../include/stt.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace stt {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 4096;     // elements per bulk-copy chunk (16 KB per array)
+constexpr int kMaxChunks = 8;
+constexpr int kSliceBudget = 81920;  // preferred shared bytes per CTA (two arrays)
+constexpr int kSliceMax = 25600;     // elements per CTA at most (200 KB)
+constexpr int kMaxCluster = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct CeParams {
+  float* z;
+  const float* p;
+  const float* g;
+  float* row_loss;
+  float* wl;
+  long long N, V;
+  int C;
+  int slice;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <bool kBulk>
+__global__ void __launch_bounds__(kThreads) soft_ce_kernel(const CeParams P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t bars[kMaxChunks];
+  __shared__ float red[3][kWarps];
+  __shared__ float redm[kWarps];
+  __shared__ __align__(16) float stats[4];
+
+  const int tid = threadIdx.x;
+  const int C = P.C;
+  const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
+  const long long row = blockIdx.x / C;
+  const long long begin = (long long)rank * P.slice;
+  const long long rem = P.V - begin;
+  const int len = rem <= 0 ? 0 : (rem < P.slice ? (int)rem : P.slice);
+  float* zrow = P.z + row * P.V + begin;
+  const float* prow = P.p + row * P.V + begin;
+  const float g = __ldg(P.g + row);
+
+  if (g == 0.0f) {
+    // Masked row: gradient is exactly 0 and nothing needs to be read.
+    if (kBulk) {
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = tid * 4; i < len; i += kThreads * 4) st_global_cs_f4(zrow + i, zero);
+    } else {
+      for (int i = tid; i < len; i += kThreads) zrow[i] = 0.0f;
+    }
+    if (rank == 0 && tid == 0) {
+      if (P.row_loss) P.row_loss[row] = 0.0f;
+      P.wl[row] = 0.0f;
+    }
+    return;
+  }
+
+  float* zs = reinterpret_cast<float*>(smem_raw);
+  float* ps = zs + P.slice;
+  const int nchunks = (len + kChunk - 1) / kChunk;
+
+  if (kBulk) {
+    if (tid == 0) {
+      for (int c = 0; c < nchunks; ++c) mbar_init(&bars[c], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int n = min(kChunk, len - c * kChunk);
+        const uint32_t bytes = (uint32_t)n * 4u;
+        mbar_arrive_expect_tx(&bars[c], 2u * bytes);
+        bulk_load(zs + c * kChunk, zrow + c * kChunk, bytes, &bars[c]);
+        bulk_load(ps + c * kChunk, prow + c * kChunk, bytes, &bars[c]);
+      }
+    }
+  } else {
+    for (int i = tid; i < len; i += kThreads) {
+      zs[i] = zrow[i];
+      ps[i] = prow[i];
+    }
+    __syncthreads();
+  }
+
+  // Pass 1: max, sum p, sum p*z over the slice.
+  float m = -INFINITY, sp = 0.f, spz = 0.f;
+  for (int c = 0; c < nchunks; ++c) {
+    const int c0 = c * kChunk;
+    const int c1 = min(len, c0 + kChunk);
+    if (kBulk) {
+      mbar_wait(&bars[c], 0, STT_DEVERR_CE_WAIT);
+      for (int i = c0 + tid * 4; i < c1; i += kThreads * 4) {
+        const float4 zv = *reinterpret_cast<const float4*>(zs + i);
+        const float4 pv = *reinterpret_cast<const float4*>(ps + i);
+        m = fmaxf(m, fmaxf(fmaxf(zv.x, zv.y), fmaxf(zv.z, zv.w)));
+        sp += (pv.x + pv.y) + (pv.z + pv.w);
+        spz = fmaf(pv.x, zv.x, spz);
+        spz = fmaf(pv.y, zv.y, spz);
+        spz = fmaf(pv.z, zv.z, spz);
+        spz = fmaf(pv.w, zv.w, spz);
+      }
+    } else {
+      for (int i = c0 + tid; i < c1; i += kThreads) {
+        const float zv = zs[i], pv = ps[i];
+        m = fmaxf(m, zv);
+        sp += pv;
+        spz = fmaf(pv, zv, spz);
+      }
+    }
+  }
+  const int warp = tid >> 5, lane = tid & 31;
+  m = warp_max(m);
+  if (lane == 0) redm[warp] = m;
+  __syncthreads();
+  m = redm[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) m = fmaxf(m, redm[w]);
+
+  // Pass 2: sum exp(z - m) over the slice (exp as 2^(z log2e - m log2e)).
+  float l = 0.f;
+  if (len > 0) {
+    const float mb = m * kLog2e;
+    if (kBulk) {
+      for (int i = tid * 4; i < len; i += kThreads * 4) {
+        const float4 zv = *reinterpret_cast<const float4*>(zs + i);
+        l += ex2(fmaf(zv.x, kLog2e, -mb)) + ex2(fmaf(zv.y, kLog2e, -mb)) +
+             ex2(fmaf(zv.z, kLog2e, -mb)) + ex2(fmaf(zv.w, kLog2e, -mb));
+      }
+    } else {
+      for (int i = tid; i < len; i += kThreads) l += ex2(fmaf(zs[i], kLog2e, -mb));
+    }
+  }
+  l = warp_sum(l);
+  sp = warp_sum(sp);
+  spz = warp_sum(spz);
+  if (lane == 0) {
+    red[0][warp] = l;
+    red[1][warp] = sp;
+    red[2][warp] = spz;
+  }
+  __syncthreads();
+  l = 0.f;
+  sp = 0.f;
+  spz = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    l += red[0][w];
+    sp += red[1][w];
+    spz += red[2][w];
+  }
+
+  // Combine the C slices of the row through distributed shared memory.
+  float M = m, Ls = l, Sp = sp, Spz = spz;
+  if (C > 1) {
+    if (tid == 0) {
+      stats[0] = m;
+      stats[1] = l;
+      stats[2] = sp;
+      stats[3] = spz;
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    float4 part[kMaxCluster];
+    M = -INFINITY;
+    for (int r = 0; r < C; ++r) {
+      part[r] = ld_shared_cluster_f4(mapa_shared(smem_u32(stats), (uint32_t)r));
+      M = fmaxf(M, part[r].x);
+    }
+    Ls = 0.f;
+    Sp = 0.f;
+    Spz = 0.f;
+    for (int r = 0; r < C; ++r) {
+      if (part[r].y > 0.f) Ls += part[r].y * ex2((part[r].x - M) * kLog2e);
+      Sp += part[r].z;
+      Spz += part[r].w;
+    }
+    // Done reading the other CTAs' statistics; the matching wait sits at the end.
+    cluster_arrive_release();
+  }
+  const float lse = M + logf(Ls);
+  const float lse2 = lse * kLog2e;
+  const float s = g * Sp;
+
+  // Pass 3: gradient from the on-chip copy, streamed to HBM.
+  if (kBulk) {
+    for (int i = tid * 4; i < len; i += kThreads * 4) {
+      const float4 zv = *reinterpret_cast<const float4*>(zs + i);
+      const float4 pv = *reinterpret_cast<const float4*>(ps + i);
+      float4 o;
+      o.x = fmaf(ex2(fmaf(zv.x, kLog2e, -lse2)), s, -pv.x * g);
+      o.y = fmaf(ex2(fmaf(zv.y, kLog2e, -lse2)), s, -pv.y * g);
+      o.z = fmaf(ex2(fmaf(zv.z, kLog2e, -lse2)), s, -pv.z * g);
+      o.w = fmaf(ex2(fmaf(zv.w, kLog2e, -lse2)), s, -pv.w * g);
+      st_global_cs_f4(zrow + i, o);
+    }
+  } else {
+    for (int i = tid; i < len; i += kThreads)
+      zrow[i] = fmaf(ex2(fmaf(zs[i], kLog2e, -lse2)), s, -ps[i] * g);
+  }
+  if (rank == 0 && tid == 0) {
+    const float ell = fmaf(lse, Sp, -Spz);
+    if (P.row_loss) P.row_loss[row] = ell;
+    P.wl[row] = g * ell;
+  }
+  if (C > 1) cluster_wait_acquire();
+}
+
+// Fixed-order sum of the per-row weighted losses (one CTA, deterministic).
+__global__ void __launch_bounds__(1024) soft_ce_loss_sum(const float* wl, long long N,
+                                                         float* loss) {
+  __shared__ double part[1024];
+  double acc = 0.0;
+  for (long long i = threadIdx.x; i < N; i += 1024) acc += (double)wl[i];
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 512; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = (float)part[0];
+}
+
+}  // namespace
+
+CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
+  (void)N;
+  CePlan plan;
+  plan.bulk = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0) &&
+              ((reinterpret_cast<uintptr_t>(p) & 15u) == 0);
+  long long C = (8 * V + kSliceBudget - 1) / kSliceBudget;
+  if (C < 1) C = 1;
+  if (C > kMaxCluster) C = kMaxCluster;
+  long long slice = (V + C - 1) / C;
+  slice = (slice + 3) / 4 * 4;
+  // Never leave a CTA of the cluster without elements when V is small.
+  while (C > 1 && (C - 1) * slice >= V) {
+    --C;
+    slice = ((V + C - 1) / C + 3) / 4 * 4;
+  }
+  plan.C = (int)C;
+  plan.slice = (int)slice;
+  plan.smem = (int)(8 * slice);
+  return plan;
+}
+
+cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const float* g,
+                           int64_t N, int64_t V, float* row_loss, float* loss, float* wl,
+                           cudaStream_t s) {
+  if (N > 0) {
+    CeParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, plan.C, plan.slice};
+    void (*kern)(const CeParams) = plan.bulk ? soft_ce_kernel<true> : soft_ce_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         plan.smem);
+    if (e != cudaSuccess) return e;
+    if (plan.C > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(N * plan.C), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)plan.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)plan.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, P);
+    if (e != cudaSuccess) return e;
+  }
+  soft_ce_loss_sum<<<1, 1024, 0, s>>>(wl, (long long)N, loss);
+  return cudaGetLastError();
+}
+
+STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)
+
+static_assert(kSliceMax * 8 <= 227 * 1024, "slice must fit in shared memory");
+static_assert((long long)kSliceMax * kMaxCluster == kCeMaxV, "max V");
+static_assert(kSliceMax <= kChunk * kMaxChunks, "chunks");
+
+}  // namespace stt

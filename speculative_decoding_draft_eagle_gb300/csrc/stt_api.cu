@@ -1,0 +1,196 @@
+// stt_api.cu -- the C ABI declared in include/stt.h: argument validation,
+// status codes, and dispatch to the kernel launchers.  No entry point
+// allocates device memory or synchronises (except stt_device_error, which is
+// documented to synchronise its stream).
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/stt.h"
+#include "internal.h"
+
+namespace stt {
+
+void* tensor_map_encoder() {
+  static void* fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = f;
+  });
+  return fn;
+}
+
+}  // namespace stt
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return STT_OK;
+  if (e == cudaErrorNotSupported) return STT_ERR_UNSUPPORTED;
+  return STT_ERR_CUDA;
+}
+
+// Shared validation of the attention arguments; fills `a` on success.
+int check_attn(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+               const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k, float scale,
+               stt::AttnArgs* a) {
+  if (!q || !k_blocks || !v_blocks || !T_host) return STT_ERR_INVALID_ARG;
+  if (B < 1 || B > STT_MAX_BATCH || H < 1 || H_kv < 1 || Q_LEN < 1) return STT_ERR_INVALID_ARG;
+  if (H % H_kv != 0) return STT_ERR_INVALID_ARG;
+  if (k < 0 || k > STT_MAX_STEP) return STT_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return STT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return STT_ERR_UNSUPPORTED;
+  if (H / H_kv > 8) return STT_ERR_UNSUPPORTED;
+  if ((long long)B * H * Q_LEN > (1ll << 31) - 1) return STT_ERR_UNSUPPORTED;
+  if (!aligned16(q)) return STT_ERR_MISALIGNED;
+  for (int j = 0; j <= k; ++j) {
+    if (!k_blocks[j] || !v_blocks[j]) return STT_ERR_INVALID_ARG;
+    if (!aligned16(k_blocks[j]) || !aligned16(v_blocks[j])) return STT_ERR_MISALIGNED;
+  }
+  for (int b = 0; b < B; ++b)
+    if (T_host[b] < 0 || T_host[b] > Q_LEN) return STT_ERR_INVALID_ARG;
+  std::memset(a, 0, sizeof(*a));
+  a->q = q;
+  for (int j = 0; j <= k; ++j) {
+    a->k_blocks[j] = k_blocks[j];
+    a->v_blocks[j] = v_blocks[j];
+  }
+  a->B = B;
+  a->H = H;
+  a->H_kv = H_kv;
+  a->D = D;
+  a->Q_LEN = Q_LEN;
+  a->k = k;
+  a->scale = scale;
+  for (int b = 0; b < B; ++b) a->T[b] = T_host[b];
+  return STT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* stt_status_string(int status) {
+  switch (status) {
+    case STT_OK: return "ok";
+    case STT_ERR_INVALID_ARG: return "invalid argument";
+    case STT_ERR_UNSUPPORTED: return "unsupported configuration";
+    case STT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case STT_ERR_CUDA: return "CUDA error";
+    case STT_ERR_TIMEOUT: return "device-side bounded wait ran out";
+    case STT_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int stt_version(void) { return 100; }
+
+int stt_device_error(void* stream, uint32_t* word) {
+  if (!word) return STT_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return STT_ERR_CUDA;
+  uint32_t w = 0, part = 0;
+  if (stt::soft_ce_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
+  w |= part;
+  if (stt::attn_fwd_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
+  w |= part;
+  if (stt::attn_bwd_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
+  w |= part;
+  *word = w;
+  return STT_OK;
+}
+
+int stt_attn_fwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                 float scale, void* out, float* lse, void* stream) {
+  try {
+    static thread_local stt::AttnArgs a;
+    int st = check_attn(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, &a);
+    if (st != STT_OK) return st;
+    if (!out || !lse) return STT_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(lse)) return STT_ERR_MISALIGNED;
+    return from_cuda(stt::attn_fwd_launch(a, out, lse, static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+size_t stt_attn_bwd_workspace_size(int B, int H, int H_kv, int D, int Q_LEN, int k) {
+  (void)H_kv;
+  (void)D;
+  (void)k;
+  if (B < 1 || H < 1 || Q_LEN < 1) return 16;
+  return stt::attn_bwd_workspace(B, H, Q_LEN);
+}
+
+int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                 float scale, const void* out, const void* dout, const float* lse, float* dq,
+                 float* const* dk_blocks, float* const* dv_blocks, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  try {
+    static thread_local stt::AttnArgs a;
+    int st = check_attn(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, &a);
+    if (st != STT_OK) return st;
+    if (!out || !dout || !lse || !dq || !dk_blocks || !dv_blocks) return STT_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq))
+      return STT_ERR_MISALIGNED;
+    stt::AttnBwdArgs g;
+    std::memset(&g, 0, sizeof(g));
+    for (int j = 0; j <= k; ++j) {
+      if (!dk_blocks[j] || !dv_blocks[j]) return STT_ERR_INVALID_ARG;
+      if (!aligned16(dk_blocks[j]) || !aligned16(dv_blocks[j])) return STT_ERR_MISALIGNED;
+      g.dk_blocks[j] = dk_blocks[j];
+      g.dv_blocks[j] = dv_blocks[j];
+    }
+    const size_t need = stt::attn_bwd_workspace(B, H, Q_LEN);
+    if (!workspace || workspace_bytes < need) return STT_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return STT_ERR_MISALIGNED;
+    g.out = out;
+    g.dout = dout;
+    g.lse = lse;
+    g.dq = dq;
+    g.delta = static_cast<float*>(workspace);
+    return from_cuda(stt::attn_bwd_launch(a, g, static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+size_t soft_ce_workspace_size(int64_t N, int64_t V) {
+  (void)V;
+  if (N < 0) return 16;
+  size_t b = (size_t)N * sizeof(float);
+  b = (b + 15) / 16 * 16;
+  return b < 16 ? 16 : b;
+}
+
+int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, int64_t N, int64_t V,
+                            float* row_loss, float* loss, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  try {
+    if (N < 0 || V < 1 || !loss) return STT_ERR_INVALID_ARG;
+    if (N > 0 && (!z || !p || !g)) return STT_ERR_INVALID_ARG;
+    if (N > 0 && V > INT64_MAX / N) return STT_ERR_INVALID_ARG;
+    if (V > stt::kCeMaxV) return STT_ERR_UNSUPPORTED;
+    if (N * (V > 16 ? 16 : V) > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < soft_ce_workspace_size(N, V)) return STT_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return STT_ERR_MISALIGNED;
+    const stt::CePlan plan = stt::soft_ce_plan(z, p, N, V);
+    if (N * (int64_t)plan.C > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    return from_cuda(stt::soft_ce_launch(plan, z, p, g, N, V, row_loss, loss,
+                                         static_cast<float*>(workspace),
+                                         static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,182 @@
+"""Python binding of the C ABI, with the same names: argument marshalling only.
+
+Every computation runs in the CUDA library; torch supplies device memory,
+streams and output allocation.  Functions take torch CUDA tensors and enqueue
+on the current torch stream (or ``stream=``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+from ._lib import check, lib
+
+__all__ = [
+    "stt_attn_fwd",
+    "stt_attn_bwd",
+    "stt_attn_bwd_workspace_size",
+    "soft_ce_fwd_bwd_inplace",
+    "soft_ce_workspace_size",
+    "stt_device_error",
+    "stt_version",
+]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _ptr_array(ts: Sequence[torch.Tensor]):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def _attn_dims(q, k_blocks, v_blocks, T):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, Q_LEN, D]")
+    B, H, Q_LEN, D = q.shape
+    if len(k_blocks) == 0 or len(k_blocks) != len(v_blocks):
+        raise ValueError("k_blocks and v_blocks must both hold k+1 tensors")
+    H_kv = k_blocks[0].shape[1]
+    _need(q, "q", torch.bfloat16)
+    for j, (kb, vb) in enumerate(zip(k_blocks, v_blocks)):
+        _need(kb, f"k_blocks[{j}]", torch.bfloat16, (B, H_kv, Q_LEN, D))
+        _need(vb, f"v_blocks[{j}]", torch.bfloat16, (B, H_kv, Q_LEN, D))
+    Tl = [int(x) for x in (T.tolist() if isinstance(T, torch.Tensor) else T)]
+    if len(Tl) != B:
+        raise ValueError("T must hold B values")
+    T_arr = (ctypes.c_int32 * B)(*Tl)
+    return B, H, H_kv, D, Q_LEN, len(k_blocks) - 1, T_arr
+
+
+def stt_attn_fwd(q: torch.Tensor, k_blocks: Sequence[torch.Tensor],
+                 v_blocks: Sequence[torch.Tensor], T, scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse-tree TTT attention forward at step k = len(k_blocks) - 1.
+
+    Returns (out bf16 [B,H,Q_LEN,D], lse fp32 [B,H,Q_LEN])."""
+    B, H, H_kv, D, Q_LEN, k, T_arr = _attn_dims(q, k_blocks, v_blocks, T)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Q_LEN), device=q.device, dtype=torch.float32)
+    _need(out, "out", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, Q_LEN))
+    ka, va = _ptr_array(k_blocks), _ptr_array(v_blocks)
+    st = lib().stt_attn_fwd(_ptr(q), ka, va, T_arr, B, H, H_kv, D, Q_LEN, k, scale, _ptr(out),
+                            _ptr(lse), _stream(stream))
+    check("stt_attn_fwd", st)
+    return out, lse
+
+
+def stt_attn_bwd_workspace_size(B, H, H_kv, D, Q_LEN, k) -> int:
+    return int(lib().stt_attn_bwd_workspace_size(B, H, H_kv, D, Q_LEN, k))
+
+
+def stt_attn_bwd(q: torch.Tensor, k_blocks: Sequence[torch.Tensor],
+                 v_blocks: Sequence[torch.Tensor], T, out: torch.Tensor, dout: torch.Tensor,
+                 lse: torch.Tensor, scale: Optional[float] = None,
+                 dq: Optional[torch.Tensor] = None, dk_blocks: Optional[List[torch.Tensor]] = None,
+                 dv_blocks: Optional[List[torch.Tensor]] = None,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of stt_attn_fwd.  Returns (dq, dk_blocks, dv_blocks), all fp32."""
+    B, H, H_kv, D, Q_LEN, k, T_arr = _attn_dims(q, k_blocks, v_blocks, T)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _need(out, "out", torch.bfloat16, q.shape)
+    _need(dout, "dout", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, Q_LEN))
+    dev = q.device
+    if dq is None:
+        dq = torch.empty(q.shape, device=dev, dtype=torch.float32)
+    kv_shape = (B, H_kv, Q_LEN, D)
+    if dk_blocks is None:
+        dk_blocks = [torch.empty(kv_shape, device=dev, dtype=torch.float32) for _ in range(k + 1)]
+    if dv_blocks is None:
+        dv_blocks = [torch.empty(kv_shape, device=dev, dtype=torch.float32) for _ in range(k + 1)]
+    _need(dq, "dq", torch.float32, q.shape)
+    for j in range(k + 1):
+        _need(dk_blocks[j], f"dk_blocks[{j}]", torch.float32, kv_shape)
+        _need(dv_blocks[j], f"dv_blocks[{j}]", torch.float32, kv_shape)
+    need = stt_attn_bwd_workspace_size(B, H, H_kv, D, Q_LEN, k)
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib().stt_attn_bwd(_ptr(q), _ptr_array(k_blocks), _ptr_array(v_blocks), T_arr, B, H,
+                            H_kv, D, Q_LEN, k, scale, _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                            _ptr_array(dk_blocks), _ptr_array(dv_blocks), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    check("stt_attn_bwd", st)
+    return dq, dk_blocks, dv_blocks
+
+
+def soft_ce_workspace_size(N: int, V: int) -> int:
+    return int(lib().soft_ce_workspace_size(N, V))
+
+
+def soft_ce_fwd_bwd_inplace(z: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
+                            row_loss: Optional[torch.Tensor] = None,
+                            loss: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, want_row_loss: bool = True,
+                            stream=None):
+    """In-place soft-CE: z is overwritten with dL/dz.  Returns (loss [1], row_loss [N] or None)."""
+    if z.dim() != 2:
+        raise ValueError("z must be [N, V]")
+    N, V = z.shape
+    _need(z, "z", torch.float32)
+    _need(p, "p", torch.float32, (N, V))
+    _need(g, "g", torch.float32, (N,))
+    dev = z.device
+    if loss is None:
+        loss = torch.empty(1, device=dev, dtype=torch.float32)
+    _need(loss, "loss", torch.float32)
+    if row_loss is None and want_row_loss:
+        row_loss = torch.empty(N, device=dev, dtype=torch.float32)
+    if row_loss is not None:
+        _need(row_loss, "row_loss", torch.float32, (N,))
+    need = soft_ce_workspace_size(N, V)
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib().soft_ce_fwd_bwd_inplace(_ptr(z), _ptr(p), _ptr(g), N, V, _ptr(row_loss),
+                                       _ptr(loss), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    check("soft_ce_fwd_bwd_inplace", st)
+    return loss, row_loss
+
+
+def stt_device_error(stream=None) -> int:
+    w = ctypes.c_uint32(0)
+    check("stt_device_error", lib().stt_device_error(_stream(stream), ctypes.byref(w)))
+    return int(w.value)
+
+
+def stt_version() -> int:
+    return int(lib().stt_version())
