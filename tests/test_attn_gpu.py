@@ -1,0 +1,137 @@
+"""GPU parity of sparse-tree TTT attention (forward and backward) against the
+fp64 oracle, through the C ABI.
+
+Tolerances (bf16 inputs, fp32 accumulation): for each of O, dQ, dK_j, dV_j
+max-abs <= 2e-2 and relative L2 <= 1e-2; lse max-abs <= 1e-3 (rows with no
+visible key must be -inf on both sides).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from speculative_decoding_draft_eagle_gb300 import ops, workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decoding_draft_eagle_gb300 import build
+    build.build()
+
+
+def f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def close(gpu, ref, name, atol=2e-2, rtol_l2=1e-2):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    d = gpu - ref
+    maxabs = float(np.abs(d).max()) if d.size else 0.0
+    nref = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(d)) / nref if nref > 0 else float(np.linalg.norm(d))
+    assert maxabs <= atol and rel <= rtol_l2, f"{name}: maxabs={maxabs:.3g} relL2={rel:.3g}"
+
+
+def close_lse(gpu, ref):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(gpu), inf_ref)
+    if (~inf_ref).any():
+        assert np.abs(gpu[~inf_ref] - ref[~inf_ref]).max() <= 1e-3
+
+
+def make(B, H, H_kv, Q, D, k, T, seed):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)  # noqa: E731
+    q = r(B, H, Q, D)
+    Ks = [r(B, H_kv, Q, D) for _ in range(k + 1)]
+    Vs = [r(B, H_kv, Q, D) for _ in range(k + 1)]
+    dO = r(B, H, Q, D)
+    return q, Ks, Vs, dO, list(T)
+
+
+def run_fwd(q, Ks, Vs, T, scale):
+    out, lse = ops.stt_attn_fwd(q.to(DEV), [x.to(DEV) for x in Ks], [x.to(DEV) for x in Vs], T,
+                                scale)
+    torch.cuda.synchronize()
+    assert ops.stt_device_error() == 0
+    return out, lse
+
+
+def check_fwd(q, Ks, Vs, T, scale, method="dense"):
+    out, lse = run_fwd(q, Ks, Vs, T, scale)
+    O_ref, lse_ref = oa.forward(f64(q), [f64(x) for x in Ks], [f64(x) for x in Vs], T, scale,
+                                method=method)
+    close(f64(out), O_ref, "O")
+    close_lse(lse.cpu().numpy(), lse_ref)
+    return out, lse
+
+
+def test_tiny_workload_forward():
+    w = wl.WORKLOADS["tiny"]
+    T, Ks, Vs, qs, dOs = wl.attn_inputs(w.attn, "cpu", w.seed)
+    k = w.attn.steps[0]
+    check_fwd(qs[k], Ks[: k + 1], Vs[: k + 1], T, w.attn.scale)
+
+
+FWD_CASES = [
+    # B, H, H_kv, Q_LEN, D, k, T
+    (1, 2, 1, 128, 64, 0, [128]),
+    (1, 2, 2, 128, 128, 0, [128]),
+    (2, 4, 2, 256, 128, 1, [256, 77]),
+    (2, 4, 1, 200, 64, 3, [0, 199]),       # T = 0 and a ragged Q_LEN
+    (1, 8, 2, 384, 128, 12, [1]),          # T = 1, long TTT
+    (3, 2, 2, 130, 128, 2, [129, 130, 2]),
+    (1, 4, 4, 64, 64, 1, [50]),            # Q_LEN smaller than one tile
+    (2, 8, 1, 512, 128, 6, [511, 300]),    # group of 8 query heads
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,Q,D,k,T", FWD_CASES)
+def test_forward_shapes(B, H, H_kv, Q, D, k, T):
+    q, Ks, Vs, _, T = make(B, H, H_kv, Q, D, k, T, seed=B * 1000 + Q + k)
+    check_fwd(q, Ks, Vs, T, 1.0 / np.sqrt(D))
+
+
+def test_forward_scale_and_large_scores():
+    """A large scale forces many running-max rescales (scores spread over ~50)."""
+    q, Ks, Vs, _, T = make(1, 2, 1, 256, 128, 2, [256], seed=5)
+    check_fwd(q, Ks, Vs, T, 0.6)
+
+
+@pytest.mark.parametrize("name", ["llama8b", "varlen", "llama70b", "long_ttt"])
+def test_forward_full_size_sampled(name):
+    """Full-size workload on the GPU; the oracle (key-set form) checks b in
+    {0, B-1} and KV groups {0, H_kv-1} with all their query heads, at the first
+    and the last TTT step."""
+    w = wl.WORKLOADS[name]
+    sh = w.attn
+    T = wl.draw_T(sh, w.seed)
+    Ks = [wl.kv_block(sh, "K", j, DEV, w.seed) for j in range(sh.n_blocks)]
+    Vs = [wl.kv_block(sh, "V", j, DEV, w.seed) for j in range(sh.n_blocks)]
+    G = sh.H // sh.H_kv
+    heads = list(range(G)) + list(range(sh.H - G, sh.H))
+    batches = sorted({0, sh.B - 1})
+    for k in (sh.steps[0], sh.steps[-1]):
+        q = wl.step_query(sh, k, DEV, w.seed)
+        out, lse = ops.stt_attn_fwd(q, Ks[: k + 1], Vs[: k + 1], T, sh.scale)
+        torch.cuda.synchronize()
+        assert ops.stt_device_error() == 0
+        for b in batches:
+            qb = f64(q[b:b + 1, heads])
+            Kb = [f64(x[b:b + 1]) for x in Ks[: k + 1]]
+            Vb = [f64(x[b:b + 1]) for x in Vs[: k + 1]]
+            # heads are renumbered 0..2G-1 inside the slice: map them onto KV heads
+            O_ref = np.zeros_like(qb)
+            l_ref = np.zeros(qb.shape[:3])
+            for i, h in enumerate(heads):
+                g = h // G
+                O1, l1 = oa.head_forward_keyset(qb[0, i], [x[0, g] for x in Kb], [x[0, g] for x in Vb],
+                                                T[b], sh.scale)
+                O_ref[0, i], l_ref[0, i] = O1, l1
+            close(f64(out[b:b + 1, heads]), O_ref, f"O[{name},k={k},b={b}]")
+            close_lse(lse[b:b + 1, heads].cpu().numpy(), l_ref)
