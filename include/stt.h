@@ -158,6 +158,29 @@ STT_API int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, in
                             float* row_loss, float* loss, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* --------------------------------------------------------------------------
+ * Per-launch timing (measurement support; no counterpart on the pages).
+ * stt_profile_start(capacity) makes every subsequent kernel launch of the
+ * library (from any thread) record a CUDA event pair around itself on its
+ * launch stream, for up to `capacity` launches.  stt_profile_stop() waits for
+ * the recorded events, writes up to `capacity` (kernel id, milliseconds)
+ * pairs into the caller's host arrays (either may be NULL), stores the count
+ * in *n and disables recording.  Events are host-side objects: no device
+ * memory is allocated.  Returns STT_ERR_INVALID_ARG when not in the right
+ * state, STT_ERR_CUDA if an event call failed.
+ * ------------------------------------------------------------------------ */
+STT_API int stt_profile_start(int capacity);
+STT_API int stt_profile_stop(int* n, int* kernel_ids, float* ms, int capacity);
+/* Static name of a kernel id ("attn_fwd", ...). */
+STT_API const char* stt_kernel_name(int kernel_id);
+
+#define STT_KERNEL_SOFT_CE 1
+#define STT_KERNEL_SOFT_CE_LOSS_SUM 2
+#define STT_KERNEL_ATTN_FWD 3
+#define STT_KERNEL_ATTN_BWD_PREP 4
+#define STT_KERNEL_ATTN_BWD_DQ 5
+#define STT_KERNEL_ATTN_BWD_DKDV 6
+
 /* Device error-word bits (sites of bounded waits). */
 #define STT_DEVERR_FWD_WAIT 0x1u
 #define STT_DEVERR_BWD_WAIT 0x2u

@@ -629,20 +629,26 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   const long long rows = (long long)a.B * a.H_kv * a.Q_LEN;
   long long blocks = (rows + 7) / 8;
   if (blocks > 152 * 32) blocks = 152 * 32;
+  prof_before(s, STT_KERNEL_ATTN_BWD_PREP);
   attn_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(P);
+  prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const unsigned grid = (unsigned)(P.n_t * a.H * a.B);
   e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DqSmem<D>::alloc);
   if (e != cudaSuccess) return e;
+  prof_before(s, STT_KERNEL_ATTN_BWD_DQ);
   attn_bwd_dq_kernel<D><<<grid, kThreads, DqSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV);
+  prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DkvSmem<D>::alloc);
   if (e != cudaSuccess) return e;
+  prof_before(s, STT_KERNEL_ATTN_BWD_DKDV);
   attn_bwd_dkdv_kernel<D><<<grid, kThreads, DkvSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV);
+  prof_after(s);
   return cudaGetLastError();
 }
 

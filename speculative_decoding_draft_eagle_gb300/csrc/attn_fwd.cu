@@ -398,7 +398,9 @@ cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(P.n_qt * a.H * a.B);
+  prof_before(s, STT_KERNEL_ATTN_FWD);
   attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(P, tmQ, tmK, tmV);
+  prof_after(s);
   return cudaGetLastError();
 }
 

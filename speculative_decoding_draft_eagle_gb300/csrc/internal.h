@@ -52,6 +52,10 @@ cudaError_t soft_ce_error_word(uint32_t* w);
 cudaError_t attn_fwd_error_word(uint32_t* w);
 cudaError_t attn_bwd_error_word(uint32_t* w);
 
+// Per-launch timing hooks (profile.cu); no-ops unless stt_profile_start ran.
+void prof_before(cudaStream_t s, int kernel_id);
+void prof_after(cudaStream_t s);
+
 // Resolves cuTensorMapEncodeTiled through the runtime (no link against libcuda).
 void* tensor_map_encoder();
 

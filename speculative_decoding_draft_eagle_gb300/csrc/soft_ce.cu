@@ -306,10 +306,14 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    prof_before(s, STT_KERNEL_SOFT_CE);
     e = cudaLaunchKernelEx(&cfg, kern, P);
+    prof_after(s);
     if (e != cudaSuccess) return e;
   }
+  prof_before(s, STT_KERNEL_SOFT_CE_LOSS_SUM);
   soft_ce_loss_sum<<<1, 1024, 0, s>>>(wl, (long long)N, loss);
+  prof_after(s);
   return cudaGetLastError();
 }
 
