@@ -22,7 +22,7 @@ soft_ce    the masked soft-target softmax cross-entropy and its in-place
            gradient (SpecForge review, §三 "内存高效梯度计算", §四
            "掩码 Softmax 损失" / "原地反向传播").
 
-Readings of the page where it is silent (each also listed in the design doc):
+Readings of the page where it is silent:
   * kv indexes the concatenation of k+1 blocks, each Q_LEN long; block 0 is
     the causal block (implied by the ``mod Q_LEN`` terms of the mask).
   * Query head h uses KV head h // (H / H_kv).

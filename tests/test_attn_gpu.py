@@ -174,7 +174,7 @@ def check_bwd(q, Ks, Vs, dO, T, scale):
 
 
 def test_tiny_workload_backward():
-    """The tiny workload at the flat the benchmark spec bound (2e-2 max-abs)."""
+    """The tiny workload at the flat bound (2e-2 max-abs)."""
     w = wl.WORKLOADS["tiny"]
     T, Ks, Vs, qs, dOs = wl.attn_inputs(w.attn, "cpu", w.seed)
     k = w.attn.steps[0]
