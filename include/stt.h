@@ -159,6 +159,32 @@ STT_API int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, in
                             size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * Allocation-free soft-CE (the paper has no counterpart; this is a library
+ * convenience).  Identical results to soft_ce_fwd_bwd_inplace, but it takes no
+ * workspace: its per-row scratch is a fixed 256 KB array inside the library
+ * (allocated when the library is loaded, held on every GPU that loads it until
+ * the process exits).  It is for callers that cannot call cudaMalloc: for
+ * example an operator plugged into a host framework that hands it only its
+ * input and output buffers and owns all device memory itself, or code in a
+ * phase where device allocation is not permitted.  The call itself allocates
+ * nothing and calls no allocating routine.
+ *
+ *  z, p, g, N, V, row_loss, loss: as soft_ce_fwd_bwd_inplace.
+ *  N must be <= 65536 rows (the scratch size); larger N returns
+ *  STT_ERR_WORKSPACE without launching anything.
+ *  The first call on a device looks up the scratch array's device address
+ *  (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *  first call before any stream capture.  All calls share the one array, so
+ *  calls whose kernels overlap on the GPU (different streams, or threads
+ *  without ordering) race on it and must be serialised by the caller.  Every
+ *  scratch entry a call reads is written earlier in the same call, so the
+ *  previous call's leftovers never affect the result.
+ * ------------------------------------------------------------------------ */
+STT_API int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const float* g, int64_t N,
+                                            int64_t V, float* row_loss, float* loss,
+                                            void* stream);
+
+/* --------------------------------------------------------------------------
  * Per-launch timing (measurement support; no counterpart on the pages).
  * stt_profile_start(capacity) makes every subsequent kernel launch of the
  * library (from any thread) record a CUDA event pair around itself on its

@@ -33,6 +33,7 @@ EXPORTS = (
     "stt_attn_bwd",
     "soft_ce_workspace_size",
     "soft_ce_fwd_bwd_inplace",
+    "soft_ce_fwd_bwd_inplace_noalloc",
     "stt_profile_start",
     "stt_profile_stop",
     "stt_kernel_name",
@@ -70,6 +71,8 @@ def _declare(L):
     L.soft_ce_workspace_size.restype = sz
     L.soft_ce_fwd_bwd_inplace.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
     L.soft_ce_fwd_bwd_inplace.restype = i32
+    L.soft_ce_fwd_bwd_inplace_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]
+    L.soft_ce_fwd_bwd_inplace_noalloc.restype = i32
     L.stt_profile_start.argtypes = [i32]
     L.stt_profile_start.restype = i32
     L.stt_profile_stop.argtypes = [c.POINTER(i32), c.POINTER(i32), c.POINTER(f32), i32]

@@ -19,6 +19,8 @@
 //   * Per-row weighted losses g_r * loss_r go to the workspace; a one-CTA kernel
 //     sums them in a fixed order, so the scalar loss is deterministic.
 #include <cmath>
+#include <cstdint>
+#include <mutex>
 
 #include "../../include/stt.h"
 #include "internal.h"
@@ -318,6 +320,71 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
 }
 
 STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the in-place soft-CE.
+//
+// The per-row weighted losses, which the regular entry point keeps in a
+// caller-provided workspace, live here in a fixed file-scope device array.
+// Every GPU that loads the library holds this array (256 KB) until the
+// process exits.  In host code `g_noalloc_scratch` is only a host-side stand-in
+// for the symbol, not a device address, so the device address is looked up
+// once per device with cudaGetSymbolAddress (with that device current) and
+// cached; kernels are always handed that looked-up pointer.
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = 65536;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocMaxRows];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on first use).
+int noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return STT_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return STT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return STT_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return STT_OK;
+}
+
+}  // namespace
+
+}  // namespace stt
+
+extern "C" int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const float* g,
+                                               int64_t N, int64_t V, float* row_loss,
+                                               float* loss, void* stream) {
+  try {
+    if (N < 0 || V < 1 || !loss) return STT_ERR_INVALID_ARG;
+    if (N > 0 && (!z || !p || !g)) return STT_ERR_INVALID_ARG;
+    if (N > 0 && V > INT64_MAX / N) return STT_ERR_INVALID_ARG;
+    if (N > stt::kNoAllocMaxRows) return STT_ERR_WORKSPACE;
+    if (V > stt::kCeMaxV) return STT_ERR_UNSUPPORTED;
+    float* scratch = nullptr;
+    const int st = stt::noalloc_scratch(&scratch);
+    if (st != STT_OK) return st;
+    // Every row of the scratch that the loss sum reads is written first by the
+    // row kernel (masked rows included), so nothing has to be cleared.
+    const stt::CePlan plan = stt::soft_ce_plan(z, p, N, V);
+    if (N * (int64_t)plan.C > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    const cudaError_t e = stt::soft_ce_launch(plan, z, p, g, N, V, row_loss, loss, scratch,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? STT_OK : STT_ERR_CUDA;
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+namespace stt {
 
 static_assert(kSliceMax * 8 <= 227 * 1024, "slice must fit in shared memory");
 static_assert((long long)kSliceMax * kMaxCluster == kCeMaxV, "max V");

@@ -20,6 +20,7 @@ __all__ = [
     "stt_attn_bwd",
     "stt_attn_bwd_workspace_size",
     "soft_ce_fwd_bwd_inplace",
+    "soft_ce_fwd_bwd_inplace_noalloc",
     "soft_ce_workspace_size",
     "stt_device_error",
     "stt_version",
@@ -169,6 +170,29 @@ def soft_ce_fwd_bwd_inplace(z: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     check("soft_ce_fwd_bwd_inplace", st)
+    return loss, row_loss
+
+
+def soft_ce_fwd_bwd_inplace_noalloc(z: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
+                                    row_loss: Optional[torch.Tensor] = None,
+                                    loss: Optional[torch.Tensor] = None, stream=None):
+    """Same as soft_ce_fwd_bwd_inplace but without a workspace: the library's own
+    fixed scratch is used (at most 65536 rows), for callers that cannot allocate
+    device memory.  Calls must not overlap on the GPU."""
+    if z.dim() != 2:
+        raise ValueError("z must be [N, V]")
+    N, V = z.shape
+    _need(z, "z", torch.float32)
+    _need(p, "p", torch.float32, (N, V))
+    _need(g, "g", torch.float32, (N,))
+    if loss is None:
+        loss = torch.empty(1, device=z.device, dtype=torch.float32)
+    _need(loss, "loss", torch.float32)
+    if row_loss is not None:
+        _need(row_loss, "row_loss", torch.float32, (N,))
+    st = lib().soft_ce_fwd_bwd_inplace_noalloc(_ptr(z), _ptr(p), _ptr(g), N, V, _ptr(row_loss),
+                                               _ptr(loss), _stream(stream))
+    check("soft_ce_fwd_bwd_inplace_noalloc", st)
     return loss, row_loss
 
 
