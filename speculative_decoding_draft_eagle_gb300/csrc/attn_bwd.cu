@@ -20,6 +20,8 @@
 //      K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T written back into TMEM as
 //      bf16, dV += P^T dO and dK += dS^T Q accumulate in TMEM over the query
 //      tiles; the group's query heads are summed with fp32 atomics.
+// In both tcgen05 kernels 8 compute warps share the element-wise phase: warps
+// w and w+4 read the same TMEM lane quarter and split its columns in halves.
 // dq is written once per row by exactly one CTA (deterministic); dK_0 / dV_0
 // sum G partials per element in arrival order.
 #include "../../include/stt.h"
@@ -28,8 +30,9 @@
 namespace stt {
 namespace {
 
-constexpr int kThreads = 192;  // warps 0-3 compute, 4 TMA, 5 MMA
-constexpr int kMaxG = 8;
+constexpr int kThreads = 320;   // warps 0-7 compute, 8 TMA, 9 MMA
+constexpr int kCompute = 256;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 
 struct BwdParams {
   const __nv_bfloat16* q;
@@ -77,7 +80,9 @@ __device__ __forceinline__ void store_f32(float* p, const float (&v)[E]) {
 }
 
 // ------------------------------------------------------------------ prep --
-template <int D>
+// GM: compile-time upper bound of the group size (the loops over heads are
+// unrolled so per-head values stay in registers); G <= GM at run time.
+template <int D, int GM>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
@@ -89,12 +94,17 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
     const int bhk = (int)(row / P.Q_LEN);
     const int b = bhk / P.H_kv, hk = bhk % P.H_kv;
     const bool valid = q < P.T[b];
-    float qv[kMaxG][E], dov[kMaxG][E], dq[kMaxG][E], lse2[kMaxG], dl[kMaxG];
+    const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + lane * E;
+    float kn[E], vn[E];
+    if (valid && P.k >= 1) {
+      load_bf16<E>(P.kb[1] + kvoff, kn);
+      load_bf16<E>(P.vb[1] + kvoff, vn);
+    }
+    float qv[GM][E], dov[GM][E], dq[GM][E], lse2[GM], dl[GM];
 #pragma unroll
-    for (int i = 0; i < kMaxG; ++i) {
+    for (int i = 0; i < GM; ++i) {
       if (i < G) {
-        const int hq = hk * G + i;
-        const size_t rq = (size_t)(b * P.H + hq) * P.Q_LEN + q;
+        const size_t rq = (size_t)(b * P.H + hk * G + i) * P.Q_LEN + q;
         const size_t off = rq * D + lane * E;
         float ov[E];
         load_bf16<E>(P.dout + off, dov[i]);
@@ -110,17 +120,23 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
         for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
       }
     }
-    const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + lane * E;
     for (int j = 1; j <= P.k; ++j) {
       float dk[E], dv[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
       if (valid) {
         float kv[E], vv[E];
-        load_bf16<E>(P.kb[j] + kvoff, kv);
-        load_bf16<E>(P.vb[j] + kvoff, vv);
 #pragma unroll
-        for (int i = 0; i < kMaxG; ++i) {
+        for (int e = 0; e < E; ++e) {
+          kv[e] = kn[e];
+          vv[e] = vn[e];
+        }
+        if (j < P.k) {  // prefetch the next block's row
+          load_bf16<E>(P.kb[j + 1] + kvoff, kn);
+          load_bf16<E>(P.vb[j + 1] + kvoff, vn);
+        }
+#pragma unroll
+        for (int i = 0; i < GM; ++i) {
           if (i < G) {
             float s = 0.f, dp = 0.f;
 #pragma unroll
@@ -146,8 +162,9 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
       store_f32<E>(P.dvb[j] + kvoff, dv);
     }
 #pragma unroll
-    for (int i = 0; i < kMaxG; ++i)
-      if (i < G) store_f32<E>(P.dq + ((size_t)(b * P.H + hk * G + i) * P.Q_LEN + q) * D + lane * E, dq[i]);
+    for (int i = 0; i < GM; ++i)
+      if (i < G)
+        store_f32<E>(P.dq + ((size_t)(b * P.H + hk * G + i) * P.Q_LEN + q) * D + lane * E, dq[i]);
     float z[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) z[e] = 0.f;
@@ -204,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_kv_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_ds_ready, 128);
+    mbar_init(&bar_ds_ready, kCompute);
     mbar_init(&bar_dq_done, 1);
     mbar_init(&bar_drain, 1);
     fence_mbar_init();
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     if (lane == 0 && n_kv > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bar_kv_full[j % NS], (uint32_t)(j / NS) & 1u, STT_DEVERR_BWD_WAIT);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     if (lane == 0 && n_kv > 0) {
       const uint32_t idSS = idesc_bf16(128, kTile, false, false);
       const uint32_t idDQ = idesc_bf16(128, D, false, true);
@@ -293,10 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
     }
   } else {
-    const int r = tid;
+    // Compute warps: row r = TMEM lane; `half` selects the 64-column half.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const int lim = causal_row_limit(qrow, T);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool in_range = qrow < P.Q_LEN;
     const size_t rq = (size_t)bh * P.Q_LEN + qrow;
     const float lse2 = in_range ? P.lse[rq] * kLog2e : 0.f;
@@ -308,25 +327,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int c0 = j * kTile;
+      uint32_t s[2][32], dp[2][32];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int cc = half * 2 + c2;
+        tmem_ld32(tmem + lane_off + kColS + cc * 32, s[c2]);
+        tmem_ld32(tmem + lane_off + kColDP + cc * 32, dp[c2]);
+      }
+      // Every compute thread holds its S / dP columns before dS overwrites S.
+      named_bar_sync(1, kCompute);
       const bool full = (c0 + kTile - 1 <= lim) && in_range;
 #pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) {
-        uint32_t s[32], dp[32], pk[16];
-        tmem_ld32(tmem + lane_off + kColS + c * 32, s);
-        tmem_ld32(tmem + lane_off + kColDP + c * 32, dp);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int cc = half * 2 + c2;
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(s[i]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(s[i + 1]), sl2, -lse2));
+          float p0 = ex2(fmaf(__uint_as_float(s[c2][i]), sl2, -lse2));
+          float p1 = ex2(fmaf(__uint_as_float(s[c2][i + 1]), sl2, -lse2));
           if (!full) {
-            if (!(in_range && c0 + c * 32 + i <= lim)) p0 = 0.f;
-            if (!(in_range && c0 + c * 32 + i + 1 <= lim)) p1 = 0.f;
+            if (!(in_range && c0 + cc * 32 + i <= lim)) p0 = 0.f;
+            if (!(in_range && c0 + cc * 32 + i + 1 <= lim)) p1 = 0.f;
           }
-          const float d0 = p0 * (__uint_as_float(dp[i]) - dlt);
-          const float d1 = p1 * (__uint_as_float(dp[i + 1]) - dlt);
+          const float d0 = p0 * (__uint_as_float(dp[c2][i]) - dlt);
+          const float d1 = p1 * (__uint_as_float(dp[c2][i + 1]) - dlt);
           pk[i >> 1] = pack_bf16(d0, d1);
         }
-        tmem_st16(tmem + lane_off + kColS + c * 16, pk);
+        tmem_st16(tmem + lane_off + kColS + cc * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -338,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         float* dqrow = P.dq + rq * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          const int c = half * (D / 64) + c2;
           uint32_t u[32];
           tmem_ld32(tmem + lane_off + kColAcc0 + c * 32, u);
           if (in_range) {
@@ -392,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_kv, bar_qdo_full[NS], bar_qdo_empty[NS], bar_sdp_full, bar_pds_ready,
       bar_acc_done, bar_drain;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_lse2[2][kTile], s_delta[2][kTile];
+  __shared__ float s_stat[2][2][kTile];  // [slot][lse2 | delta][query]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -411,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_qdo_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_pds_ready, 128);
+    mbar_init(&bar_pds_ready, kCompute);
     mbar_init(&bar_acc_done, 1);
     mbar_init(&bar_drain, 1);
     fence_mbar_init();
@@ -425,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     if (lane == 0 && n_q > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
@@ -458,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bar_qdo_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     if (lane == 0 && n_q > 0) {
       const uint32_t idSS = idesc_bf16(128, kTile, false, false);
       const uint32_t idACC = idesc_bf16(128, D, false, true);
@@ -506,44 +534,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
     }
   } else {
-    const int r = tid;
-    const int kv = c0 + r;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Compute warps: key row = TMEM lane; `half` selects the 64-query half.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int kv = c0 + quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = P.scale_log2;
     const bool kv_live = kv < T;  // T <= Q_LEN, so also kv < Q_LEN
+    // Thread tid stages one statistic of one query of the tile: lse2 (tid < 128)
+    // or Delta (tid >= 128) of query tq0 + (tid & 127); prefetched a tile ahead.
+    const int st_which = tid >> 7, st_idx = tid & 127;
+    auto fetch_stat = [&](int i) -> float {
+      const int qq = (t_first + i) * kTile + st_idx;
+      if (qq >= P.Q_LEN) return 0.f;
+      const size_t rq = (size_t)bh * P.Q_LEN + qq;
+      return st_which == 0 ? P.lse[rq] * kLog2e : P.delta[rq];
+    };
+    float stat_next = n_q > 0 ? fetch_stat(0) : 0.f;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int tq0 = (t_first + i) * kTile;
       const int slot = i & 1;
-      {
-        const int qq = tq0 + r;
-        const bool inr = qq < P.Q_LEN;
-        const size_t rq = (size_t)bh * P.Q_LEN + qq;
-        s_lse2[slot][r] = inr ? P.lse[rq] * kLog2e : 0.f;
-        s_delta[slot][r] = inr ? P.delta[rq] : 0.f;
-      }
-      named_bar_sync(1, 128);
+      s_stat[slot][st_which][st_idx] = stat_next;
+      if (i + 1 < n_q) stat_next = fetch_stat(i + 1);
+      named_bar_sync(1, kCompute);
       ok = warp_wait(&bar_sdp_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
+      uint32_t s[2][32], dp[2][32];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int cc = half * 2 + c2;
+        tmem_ld32(tmem + lane_off + kColS + cc * 32, s[c2]);
+        tmem_ld32(tmem + lane_off + kColDP + cc * 32, dp[c2]);
+      }
+      // Every compute thread holds its S^T / dP^T columns before they are overwritten.
+      named_bar_sync(1, kCompute);
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
       const bool full = kv_live && kv <= tq0 && tq0 + kTile <= P.Q_LEN;
+      const float* lse_s = s_stat[slot][0];
+      const float* dl_s = s_stat[slot][1];
 #pragma unroll
-      for (int cc = 0; cc < kTile / 32; ++cc) {
-        uint32_t s[32], dp[32], pp[16], dd[16];
-        tmem_ld32(tmem + lane_off + kColS + cc * 32, s);
-        tmem_ld32(tmem + lane_off + kColDP + cc * 32, dp);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int cc = half * 2 + c2;
+        uint32_t pp[16], dd[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const int qa = tq0 + cc * 32 + x;
-          float p0 = ex2(fmaf(__uint_as_float(s[x]), sl2, -s_lse2[slot][cc * 32 + x]));
-          float p1 = ex2(fmaf(__uint_as_float(s[x + 1]), sl2, -s_lse2[slot][cc * 32 + x + 1]));
+          const int ql = cc * 32 + x;
+          const int qa = tq0 + ql;
+          float p0 = ex2(fmaf(__uint_as_float(s[c2][x]), sl2, -lse_s[ql]));
+          float p1 = ex2(fmaf(__uint_as_float(s[c2][x + 1]), sl2, -lse_s[ql + 1]));
           if (!full) {
             if (!(kv_live && kv <= qa && qa < P.Q_LEN)) p0 = 0.f;
             if (!(kv_live && kv <= qa + 1 && qa + 1 < P.Q_LEN)) p1 = 0.f;
           }
-          const float d0 = p0 * (__uint_as_float(dp[x]) - s_delta[slot][cc * 32 + x]);
-          const float d1 = p1 * (__uint_as_float(dp[x + 1]) - s_delta[slot][cc * 32 + x + 1]);
+          const float d0 = p0 * (__uint_as_float(dp[c2][x]) - dl_s[ql]);
+          const float d1 = p1 * (__uint_as_float(dp[c2][x + 1]) - dl_s[ql + 1]);
           pp[x >> 1] = pack_bf16(p0, p1);
           dd[x >> 1] = pack_bf16(d0, d1);
         }
@@ -562,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* dkr = P.dkb[0] + off;
         float* dvr = P.dvb[0] + off;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          const int cc = half * (D / 64) + c2;
           uint32_t uv[32], uk[32];
           tmem_ld32(tmem + lane_off + kColAcc0 + cc * 32, uv);
           tmem_ld32(tmem + lane_off + kColAcc1 + cc * 32, uk);
@@ -589,6 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <int D, int GM>
+void launch_prep(const BwdParams& P, long long blocks, cudaStream_t s) {
+  attn_bwd_prep_kernel<D, GM><<<(unsigned)blocks, 256, 0, s>>>(P);
 }
 
 template <int D>
@@ -630,7 +681,14 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   long long blocks = (rows + 7) / 8;
   if (blocks > 152 * 32) blocks = 152 * 32;
   prof_before(s, STT_KERNEL_ATTN_BWD_PREP);
-  attn_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(P);
+  if (P.G == 1)
+    launch_prep<D, 1>(P, blocks, s);
+  else if (P.G == 2)
+    launch_prep<D, 2>(P, blocks, s);
+  else if (P.G <= 4)
+    launch_prep<D, 4>(P, blocks, s);
+  else
+    launch_prep<D, 8>(P, blocks, s);
   prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
