@@ -95,11 +95,6 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
     const int b = bhk / P.H_kv, hk = bhk % P.H_kv;
     const bool valid = q < P.T[b];
     const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + lane * E;
-    float kn[E], vn[E];
-    if (valid && P.k >= 1) {
-      load_bf16<E>(P.kb[1] + kvoff, kn);
-      load_bf16<E>(P.vb[1] + kvoff, vn);
-    }
     float qv[GM][E], dov[GM][E], dq[GM][E], lse2[GM], dl[GM];
 #pragma unroll
     for (int i = 0; i < GM; ++i) {
@@ -120,46 +115,54 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
         for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
       }
     }
-    for (int j = 1; j <= P.k; ++j) {
-      float dk[E], dv[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
+    // Blocks are taken kJ at a time with all their row loads issued up front, so
+    // each warp keeps 2*kJ loads in flight.
+    constexpr int kJ = 4;
+    for (int j0 = 1; j0 <= P.k; j0 += kJ) {
+      float kv[kJ][E], vv[kJ][E];
       if (valid) {
-        float kv[E], vv[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          kv[e] = kn[e];
-          vv[e] = vn[e];
-        }
-        if (j < P.k) {  // prefetch the next block's row
-          load_bf16<E>(P.kb[j + 1] + kvoff, kn);
-          load_bf16<E>(P.vb[j + 1] + kvoff, vn);
-        }
-#pragma unroll
-        for (int i = 0; i < GM; ++i) {
-          if (i < G) {
-            float s = 0.f, dp = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-              s = fmaf(qv[i][e], kv[e], s);
-              dp = fmaf(dov[i][e], vv[e], dp);
-            }
-            s = warp_sum(s);
-            dp = warp_sum(dp);
-            const float p = ex2(s * P.scale_log2 - lse2[i]);
-            const float ds = p * (dp - dl[i]);
-            const float dss = ds * P.scale;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-              dq[i][e] = fmaf(dss, kv[e], dq[i][e]);
-              dk[e] = fmaf(dss, qv[i][e], dk[e]);
-              dv[e] = fmaf(p, dov[i][e], dv[e]);
-            }
+        for (int u = 0; u < kJ; ++u) {
+          if (j0 + u <= P.k) {
+            load_bf16<E>(P.kb[j0 + u] + kvoff, kv[u]);
+            load_bf16<E>(P.vb[j0 + u] + kvoff, vv[u]);
           }
         }
       }
-      store_f32<E>(P.dkb[j] + kvoff, dk);
-      store_f32<E>(P.dvb[j] + kvoff, dv);
+#pragma unroll
+      for (int u = 0; u < kJ; ++u) {
+        const int j = j0 + u;
+        if (j > P.k) break;
+        float dk[E], dv[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < GM; ++i) {
+            if (i < G) {
+              float s = 0.f, dp = 0.f;
+#pragma unroll
+              for (int e = 0; e < E; ++e) {
+                s = fmaf(qv[i][e], kv[u][e], s);
+                dp = fmaf(dov[i][e], vv[u][e], dp);
+              }
+              s = warp_sum(s);
+              dp = warp_sum(dp);
+              const float p = ex2(s * P.scale_log2 - lse2[i]);
+              const float ds = p * (dp - dl[i]);
+              const float dss = ds * P.scale;
+#pragma unroll
+              for (int e = 0; e < E; ++e) {
+                dq[i][e] = fmaf(dss, kv[u][e], dq[i][e]);
+                dk[e] = fmaf(dss, qv[i][e], dk[e]);
+                dv[e] = fmaf(p, dov[i][e], dv[e]);
+              }
+            }
+          }
+        }
+        store_f32<E>(P.dkb[j] + kvoff, dk);
+        store_f32<E>(P.dvb[j] + kvoff, dv);
+      }
     }
 #pragma unroll
     for (int i = 0; i < GM; ++i)
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_qdo, bar_kv_full[NS], bar_kv_empty[NS], bar_sdp_full, bar_ds_ready,
-      bar_dq_done, bar_drain;
+      bar_dq_done, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_ds_ready, kCompute);
     mbar_init(&bar_dq_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_grp, kCompute);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -321,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = in_range ? P.lse[rq] * kLog2e : 0.f;
     const float dlt = in_range ? P.delta[rq] : 0.f;
     const float sl2 = P.scale_log2;
+    uint32_t grp_uses = 0;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = warp_wait(&bar_sdp_full, (uint32_t)j & 1u, STT_DEVERR_BWD_WAIT);
@@ -328,14 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int c0 = j * kTile;
       uint32_t s[2][32], dp[2][32];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int cc = half * 2 + c2;
-        tmem_ld32(tmem + lane_off + kColS + cc * 32, s[c2]);
-        tmem_ld32(tmem + lane_off + kColDP + cc * 32, dp[c2]);
-      }
+      tmem_ld64x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColDP + half * 64, s[0],
+                  s[1], dp[0], dp[1]);
       // Every compute thread holds its S / dP columns before dS overwrites S.
-      named_bar_sync(1, kCompute);
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
       const bool full = (c0 + kTile - 1 <= lim) && in_range;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_kv, bar_qdo_full[NS], bar_qdo_empty[NS], bar_sdp_full, bar_pds_ready,
-      bar_acc_done, bar_drain;
+      bar_acc_done, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
   __shared__ float s_stat[2][2][kTile];  // [slot][lse2 | delta][query]
 
@@ -442,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_pds_ready, kCompute);
     mbar_init(&bar_acc_done, 1);
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_grp, kCompute);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -550,25 +553,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       return st_which == 0 ? P.lse[rq] * kLog2e : P.delta[rq];
     };
     float stat_next = n_q > 0 ? fetch_stat(0) : 0.f;
+    uint32_t grp_uses = 0;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       const int tq0 = (t_first + i) * kTile;
       const int slot = i & 1;
       s_stat[slot][st_which][st_idx] = stat_next;
       if (i + 1 < n_q) stat_next = fetch_stat(i + 1);
-      named_bar_sync(1, kCompute);
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
       ok = warp_wait(&bar_sdp_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[2][32], dp[2][32];
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int cc = half * 2 + c2;
-        tmem_ld32(tmem + lane_off + kColS + cc * 32, s[c2]);
-        tmem_ld32(tmem + lane_off + kColDP + cc * 32, dp[c2]);
-      }
+      tmem_ld64x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColDP + half * 64, s[0],
+                  s[1], dp[0], dp[1]);
       // Every compute thread holds its S^T / dP^T columns before they are overwritten.
-      named_bar_sync(1, kCompute);
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
       const bool full = kv_live && kv <= tq0 && tq0 + kTile <= P.Q_LEN;
       const float* lse_s = s_stat[slot][0];
@@ -610,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c2 = 0; c2 < D / 64; ++c2) {
           const int cc = half * (D / 64) + c2;
           uint32_t uv[32], uk[32];
-          tmem_ld32(tmem + lane_off + kColAcc0 + cc * 32, uv);
-          tmem_ld32(tmem + lane_off + kColAcc1 + cc * 32, uk);
+          tmem_ld32x2(tmem + lane_off + kColAcc0 + cc * 32, tmem + lane_off + kColAcc1 + cc * 32,
+                      uv, uk);
           if (kv_live) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {

@@ -61,6 +61,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// Bounded barrier among the threads counted by `bar` (an mbarrier initialised
+// with that count).  Unlike a named hardware barrier it cannot deadlock when
+// some thread gave up on an earlier bounded wait: the others time out too.
+// `uses` counts this thread's completed phases (same sequence in every thread).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& uses, uint32_t site) {
+  mbar_arrive(bar);
+  const bool ok = warp_wait(bar, uses & 1u, site);
+  ++uses;
+  return ok;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

@@ -8,17 +8,23 @@
 //     O += P V accumulate in tensor memory (TMEM), fully masked key tiles are
 //     never visited and the padded columns kv >= T are cut (tile count and
 //     per-element limit);
-//   * folds the k diagonal suffix keys into the same online softmax as per-row
-//     dot products (CUDA cores): their scores seed the running max / sum
-//     before the first tile, and their V rows are added in the epilogue.
+//   * then folds the k diagonal suffix keys into the same online softmax as
+//     per-row dot products on CUDA cores: TMA brings rows q0..q0+127 of K_j and
+//     V_j (the only rows this query tile needs) into shared memory, and each
+//     thread updates its O row (held in registers) with one key per block.
+//     The online softmax is order independent, so taking the suffix keys last
+//     gives the same result as any other order.
 //
-// Warp roles (192 threads, one CTA per 128-row query tile of one head):
-//   warps 0-3  softmax: thread r owns query row q0+r (= TMEM lane r); loads S
-//              from TMEM, masks, exponentiates, writes P (bf16) to shared
-//              memory, rescales O in TMEM when the running max grows by more
-//              than 2^8, and writes O / lse in the epilogue.
-//   warp 4     TMA producer (one lane): Q once, then K/V tiles, 2 stages.
-//   warp 5     MMA issuer (one lane): S(j) into one of two TMEM buffers, then
+// Warp roles (320 threads, one CTA per 128-row query tile of one head):
+//   warps 0-7  softmax: warps w and w+4 own the 32 query rows of TMEM lane
+//              quarter w%4 and split the 128 key columns (and O's D columns)
+//              in halves; the row max is exchanged through shared memory.
+//              They load S from TMEM, mask, exponentiate, write P (bf16) to
+//              shared memory, rescale O in TMEM when the running max grows by
+//              more than 2^8, and finish with the suffix keys and O / lse.
+//   warp 8     TMA producer (one lane): Q once, then K/V tiles (2 stages),
+//              then the suffix K_j / V_j tiles through the same buffers.
+//   warp 9     MMA issuer (one lane): S(j) into one of two TMEM buffers, then
 //              O += P(j-1) V(j-1), so S(j+1) overlaps the softmax of tile j.
 #include "../../include/stt.h"
 #include "attn_common.cuh"
@@ -27,18 +33,23 @@ namespace stt {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmax = 256;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
 
 struct FwdParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* kb[kMaxBlocks];
-  const __nv_bfloat16* vb[kMaxBlocks];
   __nv_bfloat16* out;
   float* lse;
   int B, H, H_kv, Q_LEN, k, n_qt, G;
   float scale_log2;
   int T[kMaxBatch];
+};
+
+// Tensor maps of the later blocks' keys and values (j = 1..k).
+struct SfxMaps {
+  CUtensorMap k[kMaxBlocks - 1];
+  CUtensorMap v[kMaxBlocks - 1];
 };
 
 template <int D>
@@ -58,18 +69,42 @@ struct FwdSmem {
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256;
 
+// Dot product of row r of two swizzled [128 x D] bf16 tiles in shared memory.
+template <int D>
+__device__ __forceinline__ float smem_row_dot(const unsigned char* a, const unsigned char* b, int r) {
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint32_t off = swz_chunk_offset(r, c, kTile);
+    const uint4 x = *reinterpret_cast<const uint4*>(a + off);
+    const uint4 y = *reinterpret_cast<const uint4*>(b + off);
+    acc0 = fmaf(bf16lo(x.x), bf16lo(y.x), acc0);
+    acc1 = fmaf(bf16hi(x.x), bf16hi(y.x), acc1);
+    acc0 = fmaf(bf16lo(x.y), bf16lo(y.y), acc0);
+    acc1 = fmaf(bf16hi(x.y), bf16hi(y.y), acc1);
+    acc0 = fmaf(bf16lo(x.z), bf16lo(y.z), acc0);
+    acc1 = fmaf(bf16hi(x.z), bf16hi(y.z), acc1);
+    acc0 = fmaf(bf16lo(x.w), bf16lo(y.w), acc0);
+    acc1 = fmaf(bf16hi(x.w), bf16hi(y.w), acc1);
+  }
+  return acc0 + acc1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams P, const __grid_constant__ CUtensorMap tmQ,
-                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ SfxMaps sfx) {
   using L = FwdSmem<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
-      bar_v_empty[kStages], bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_done, bar_drain;
+      bar_v_empty[kStages], bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_done, bar_drain,
+      bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
+  __shared__ float s_sum[2][kTile];     // [half][row] partial row sum
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -80,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = t * kTile;
   const int T = P.T[b];
   const int n_kv = causal_kv_tiles(q0, T);
+  const int n_sfx = (q0 < T) ? P.k : 0;  // suffix blocks this tile needs (q0 < T => n_kv >= 1)
 
   if (tid == 0) {
     mbar_init(&bar_q, 1);
@@ -88,15 +124,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_v_full[s], 1);
       mbar_init(&bar_k_empty[s], 1);
       mbar_init(&bar_v_empty[s], 1);
+      mbar_init(&bar_sfx_full[s], 1);
+      mbar_init(&bar_sfx_empty[s], kSoftmax);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_free[s], 128);
+      mbar_init(&bar_s_free[s], kSoftmax);
     }
-    mbar_init(&bar_p_full, 128);
+    mbar_init(&bar_p_full, kSoftmax);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
-    abort_flag = 0;
+    mbar_init(&bar_grp, kSoftmax);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -110,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sQ = smem + L::q;
   unsigned char* sP = smem + L::p;
 
-  if (warp == 4) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_kv > 0) {
       tma_prefetch_desc(&tmQ);
@@ -120,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bar_q, L::kQ);
       for (int cb = 0; cb < D / kColBlock; ++cb)
         tma_load_3d(sQ + cb * kTile * 128, &tmQ, &bar_q, cb * kColBlock, q0, bh);
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStages;
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
@@ -129,29 +167,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < D / kColBlock; ++cb)
           tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &tmK, &bar_k_full[st],
                       cb * kColBlock, j * kTile, bhk);
-        if (j >= kStages && !mbar_wait(&bar_v_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) {
-          ++issued;
-          break;
-        }
+        ++issued_k;
+        if (j >= kStages && !mbar_wait(&bar_v_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) break;
         mbar_arrive_expect_tx(&bar_v_full[st], L::kKV);
         for (int cb = 0; cb < D / kColBlock; ++cb)
           tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &tmV, &bar_v_full[st],
                       cb * kColBlock, j * kTile, bhk);
-        ++issued;
+        ++issued_v;
       }
-      if (issued < n_kv) {
-        // Gave up: let every copy already issued land before the CTA exits.
-        abort_flag = 1;
-        mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
-        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-          const int st = j % kStages;
-          const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-          mbar_wait(&bar_k_full[st], ph, STT_DEVERR_FWD_WAIT);
-          mbar_wait(&bar_v_full[st], ph, STT_DEVERR_FWD_WAIT);
+      int issued_s = 0;
+      bool ok = issued_v == n_kv;
+      // Suffix tiles reuse the K/V stage buffers once every MMA has finished.
+      if (ok && n_sfx > 0) ok = mbar_wait(&bar_drain, 0, STT_DEVERR_FWD_WAIT);
+      for (int j = 1; ok && j <= n_sfx; ++j) {
+        const int st = (j - 1) % kStages;
+        const uint32_t ph = (uint32_t)((j - 1) / kStages) & 1u;
+        if (j > kStages && !mbar_wait(&bar_sfx_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx(&bar_sfx_full[st], 2 * L::kKV);
+        for (int cb = 0; cb < D / kColBlock; ++cb) {
+          tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &sfx.k[j - 1],
+                      &bar_sfx_full[st], cb * kColBlock, q0, bhk);
+          tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &sfx.v[j - 1],
+                      &bar_sfx_full[st], cb * kColBlock, q0, bhk);
+        }
+        ++issued_s;
       }
+      if (issued_v < n_kv) {
+        // Gave up: let every copy already issued land before the CTA exits.
+        mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
+        for (int j = (issued_k > kStages ? issued_k - kStages : 0); j < issued_k; ++j)
+          mbar_wait(&bar_k_full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+        for (int j = (issued_v > kStages ? issued_v - kStages : 0); j < issued_v; ++j)
+          mbar_wait(&bar_v_full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+      }
+      if (!ok)
+        for (int i = (issued_s > kStages ? issued_s - kStages : 0); i < issued_s; ++i)
+          mbar_wait(&bar_sfx_full[i % kStages], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && n_kv > 0) {
       const uint32_t idS = idesc_bf16(128, kTile, false, false);
@@ -194,67 +250,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) ok = issue_pv(n_kv - 1);
-      if (!ok) abort_flag = 1;
-      // Every MMA issued by this thread is complete before TMEM is released.
+      // Every MMA issued by this thread is complete before TMEM or the stage
+      // buffers are reused.
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_FWD_WAIT);
     }
   } else {
     // ------------------------------------------------------------ softmax --
-    const int r = tid;  // 0..127 = TMEM lane = query row in the tile
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // query row in the tile = TMEM lane
     const int qrow = q0 + r;
     const int lim = causal_row_limit(qrow, T);
-    const bool sfx_row = qrow < T;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = P.scale_log2;
-    const size_t row_kv = ((size_t)(b * P.H_kv + hk) * P.Q_LEN + qrow) * D;
+    uint32_t grp_uses = 0;
 
-    // Suffix keys (one per later block) seed the running max and sum.
     float m_run = -INFINITY, l_run = 0.f;
-    float sfx[kMaxBlocks - 1];
-    if (sfx_row) {
-      const __nv_bfloat16* qp = P.q + ((size_t)bh * P.Q_LEN + qrow) * D;
-      for (int j = 1; j <= P.k; ++j) {
-        const float s = dot_bf16_rows<D>(qp, P.kb[j] + row_kv) * sl2;
-        sfx[j - 1] = s;
-        m_run = fmaxf(m_run, s);
-      }
-      for (int j = 1; j <= P.k; ++j) l_run += ex2(sfx[j - 1] - m_run);
-    }
-
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int sb = j & 1;
       ok = warp_wait(&bar_s_full[sb], (uint32_t)(j >> 1) & 1u, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[kTile / 32][32];
-#pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) tmem_ld32(tmem + lane_off + kColS0 + sb * kTile + c * 32, s[c]);
+      uint32_t s[2][32];
+      tmem_ld32x2(tmem + lane_off + kColS0 + sb * kTile + half * 64,
+                  tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
       tc_fence_before();
       mbar_arrive(&bar_s_free[sb]);
 
-      const int c0 = j * kTile;
+      const int cbase = j * kTile + half * 64;
       float mt = -INFINITY;
-      if (c0 + kTile - 1 <= lim) {
+      if (cbase + 63 <= lim) {
 #pragma unroll
-        for (int c = 0; c < kTile / 32; ++c)
+        for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(s[c][i]) * sl2;
-            s[c][i] = __float_as_uint(x);
+            const float x = __uint_as_float(s[c2][i]) * sl2;
+            s[c2][i] = __float_as_uint(x);
             mt = fmaxf(mt, x);
           }
       } else {
 #pragma unroll
-        for (int c = 0; c < kTile / 32; ++c)
+        for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x = (c0 + c * 32 + i <= lim) ? __uint_as_float(s[c][i]) * sl2 : -INFINITY;
-            s[c][i] = __float_as_uint(x);
+            const float x = (cbase + c2 * 32 + i <= lim) ? __uint_as_float(s[c2][i]) * sl2 : -INFINITY;
+            s[c2][i] = __float_as_uint(x);
             mt = fmaxf(mt, x);
           }
       }
+      // Combine the two halves' maxima (buffer double-buffered by tile parity).
+      s_max[sb][half][r] = mt;
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
+      if (!ok) break;
+      mt = fmaxf(mt, s_max[sb][half ^ 1][r]);
+
       float alpha = 1.f;
       bool rescale_o = false;
       const float m_new = fmaxf(m_run, mt);
@@ -265,16 +315,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale_o = j > 0;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[kTile / 2];
+      uint32_t pk[32];
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < kTile / 32; ++c)
+      for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2(__uint_as_float(s[c][i]) - m_use);
-          const float p1 = ex2(__uint_as_float(s[c][i + 1]) - m_use);
+          const float p0 = ex2(__uint_as_float(s[c2][i]) - m_use);
+          const float p1 = ex2(__uint_as_float(s[c2][i + 1]) - m_use);
           rs += p0 + p1;
-          pk[(c * 32 + i) >> 1] = pack_bf16(p0, p1);
+          pk[(c2 * 32 + i) >> 1] = pack_bf16(p0, p1);
         }
       l_run += rs;
 
@@ -285,9 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c2 = 0; c2 < D / 64; ++c2) {
           uint32_t o[32];
-          const uint32_t addr = tmem + lane_off + kColO + c * 32;
+          const uint32_t addr = tmem + lane_off + kColO + (half * (D / 64) + c2) * 32;
           tmem_ld32(addr, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
@@ -295,11 +345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P row -> swizzled K-major tile (A operand of O += P V).
+      // P row half -> swizzled K-major tile (A operand of O += P V).
 #pragma unroll
-      for (int c = 0; c < kTile / 8; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sP + swz_chunk_offset(r, c, kTile)) = v;
+        *reinterpret_cast<uint4*>(sP + swz_chunk_offset(r, half * 8 + c, kTile)) = v;
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -309,55 +359,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&bar_o_done, (uint32_t)(n_kv - 1) & 1u, STT_DEVERR_FWD_WAIT);
       tc_fence_after();
     }
-    if (!ok) abort_flag = 1;
 
-    // ----------------------------------------------------------- epilogue --
-    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    if (sfx_row)
-      for (int j = 1; j <= P.k; ++j) sfx[j - 1] = ex2(sfx[j - 1] - m_use);
-    __nv_bfloat16* orow = P.out + ((size_t)bh * P.Q_LEN + qrow) * D;
-    const bool in_range = qrow < P.Q_LEN;
+    // This thread's half of the O row, in registers.
+    constexpr int DH = D / 2;
+    float o[DH];
+    if (ok && n_kv > 0) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      float o[32];
-      if (ok && n_kv > 0) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + kColO + c * 32, u);
+      for (int c2 = 0; c2 < DH / 32; c2 += 2) {
+        uint32_t u0[32], u1[32];
+        const uint32_t a0 = tmem + lane_off + kColO + half * DH + c2 * 32;
+        if (DH / 32 >= 2) {
+          tmem_ld32x2(a0, a0 + 32, u0, u1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(u[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-      }
-      if (sfx_row) {
-        for (int j = 1; j <= P.k; ++j) {
-          const uint4* vp = reinterpret_cast<const uint4*>(P.vb[j] + row_kv + c * 32);
-          const float w = sfx[j - 1];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 x = __ldg(vp + q4);
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              o[q4 * 8 + 2 * e] = fmaf(w, bf16lo(xs[e]), o[q4 * 8 + 2 * e]);
-              o[q4 * 8 + 2 * e + 1] = fmaf(w, bf16hi(xs[e]), o[q4 * 8 + 2 * e + 1]);
-            }
+          for (int i = 0; i < 32; ++i) {
+            o[c2 * 32 + i] = __uint_as_float(u0[i]);
+            if (c2 * 32 + 32 + i < DH) o[c2 * 32 + 32 + i] = __uint_as_float(u1[i]);
           }
+        } else {
+          tmem_ld32(a0, u0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = __uint_as_float(u0[i]);
         }
       }
-      if (in_range) {
-        uint4* op = reinterpret_cast<uint4*>(orow + c * 32);
+    } else {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          op[q4] = make_uint4(pack_bf16(o[q4 * 8 + 0] * inv_l, o[q4 * 8 + 1] * inv_l),
-                              pack_bf16(o[q4 * 8 + 2] * inv_l, o[q4 * 8 + 3] * inv_l),
-                              pack_bf16(o[q4 * 8 + 4] * inv_l, o[q4 * 8 + 5] * inv_l),
-                              pack_bf16(o[q4 * 8 + 6] * inv_l, o[q4 * 8 + 7] * inv_l));
+      for (int i = 0; i < DH; ++i) o[i] = 0.f;
+    }
+
+    // ------------------------------------------- suffix keys (blocks 1..k) --
+    // Query q < T sees key q of every later block: one score per block, a
+    // register-level online-softmax update of this thread's O half.
+    const bool sfx_row = qrow < T;
+    for (int j = 1; ok && j <= n_sfx; ++j) {
+      const int st = (j - 1) % kStages;
+      ok = warp_wait(&bar_sfx_full[st], (uint32_t)((j - 1) / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+      if (!ok) break;
+      if (sfx_row) {
+        const unsigned char* sK = smem + L::k0 + st * L::kKV;
+        const unsigned char* sV = smem + L::v0 + st * L::kKV;
+        const float sj = smem_row_dot<D>(sQ, sK, r) * sl2;
+        if (sj > m_run) {
+          const float alpha = ex2(m_run - sj);  // 0 when m_run is -inf
+          l_run *= alpha;
+#pragma unroll
+          for (int i = 0; i < DH; ++i) o[i] *= alpha;
+          m_run = sj;
+        }
+        const float pj = ex2(sj - m_run);
+        if (half == 0) l_run += pj;
+#pragma unroll
+        for (int c = 0; c < DH / 8; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sV + swz_chunk_offset(r, half * (DH / 8) + c, kTile));
+          o[c * 8 + 0] = fmaf(pj, bf16lo(x.x), o[c * 8 + 0]);
+          o[c * 8 + 1] = fmaf(pj, bf16hi(x.x), o[c * 8 + 1]);
+          o[c * 8 + 2] = fmaf(pj, bf16lo(x.y), o[c * 8 + 2]);
+          o[c * 8 + 3] = fmaf(pj, bf16hi(x.y), o[c * 8 + 3]);
+          o[c * 8 + 4] = fmaf(pj, bf16lo(x.z), o[c * 8 + 4]);
+          o[c * 8 + 5] = fmaf(pj, bf16hi(x.z), o[c * 8 + 5]);
+          o[c * 8 + 6] = fmaf(pj, bf16lo(x.w), o[c * 8 + 6]);
+          o[c * 8 + 7] = fmaf(pj, bf16hi(x.w), o[c * 8 + 7]);
+        }
+      }
+      mbar_arrive(&bar_sfx_empty[st]);
+    }
+
+    // ----------------------------------------------------------- epilogue --
+    if (ok) {
+      s_sum[half][r] = l_run;
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
+      l_run += s_sum[half ^ 1][r];
+    }
+    if (ok) {
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      if (qrow < P.Q_LEN) {
+        uint4* op = reinterpret_cast<uint4*>(P.out + ((size_t)bh * P.Q_LEN + qrow) * D + half * DH);
+#pragma unroll
+        for (int c = 0; c < DH / 8; ++c)
+          op[c] = make_uint4(pack_bf16(o[c * 8 + 0] * inv_l, o[c * 8 + 1] * inv_l),
+                             pack_bf16(o[c * 8 + 2] * inv_l, o[c * 8 + 3] * inv_l),
+                             pack_bf16(o[c * 8 + 4] * inv_l, o[c * 8 + 5] * inv_l),
+                             pack_bf16(o[c * 8 + 6] * inv_l, o[c * 8 + 7] * inv_l));
+        if (half == 0)
+          P.lse[(size_t)bh * P.Q_LEN + qrow] =
+              l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       }
     }
-    if (in_range)
-      P.lse[(size_t)bh * P.Q_LEN + qrow] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
@@ -371,18 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   CUtensorMap tmQ, tmK, tmV;
+  static thread_local SfxMaps sfx;
   cudaError_t e;
   if ((e = encode_tile_map(&tmQ, a.q, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmK, a.k_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
   if ((e = encode_tile_map(&tmV, a.v_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
-  static thread_local FwdParams P;
-  P.q = static_cast<const __nv_bfloat16*>(a.q);
-  for (int j = 0; j < kMaxBlocks; ++j) {
-    P.kb[j] = static_cast<const __nv_bfloat16*>(a.k_blocks[j]);
-    P.vb[j] = static_cast<const __nv_bfloat16*>(a.v_blocks[j]);
+  for (int j = 1; j <= a.k; ++j) {
+    if ((e = encode_tile_map(&sfx.k[j - 1], a.k_blocks[j], D, a.Q_LEN, a.B * a.H_kv, kTile)) !=
+        cudaSuccess)
+      return e;
+    if ((e = encode_tile_map(&sfx.v[j - 1], a.v_blocks[j], D, a.Q_LEN, a.B * a.H_kv, kTile)) !=
+        cudaSuccess)
+      return e;
   }
+  static thread_local FwdParams P;
   P.out = static_cast<__nv_bfloat16*>(out);
   P.lse = lse;
   P.B = a.B;
@@ -399,7 +489,7 @@ cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(P.n_qt * a.H * a.B);
   prof_before(s, STT_KERNEL_ATTN_FWD);
-  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(P, tmQ, tmK, tmV);
+  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(P, tmQ, tmK, tmV, sfx);
   prof_after(s);
   return cudaGetLastError();
 }
