@@ -204,8 +204,7 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_KERNEL_SOFT_CE_LOSS_SUM 2
 #define STT_KERNEL_ATTN_FWD 3
 #define STT_KERNEL_ATTN_BWD_PREP 4
-#define STT_KERNEL_ATTN_BWD_DQ 5
-#define STT_KERNEL_ATTN_BWD_DKDV 6
+#define STT_KERNEL_ATTN_BWD_CAUSAL 5
 
 /* Device error-word bits (sites of bounded waits). */
 #define STT_DEVERR_FWD_WAIT 0x1u

@@ -7,23 +7,24 @@
 //     Delta_q = sum_d dO * O,  P = exp(S - lse),  dS = P (dP - Delta),
 //     dq = scale dS Kc,  dKc = scale dS^T q,  dVc = P^T dO.
 //
-// Three kernels, in stream order:
+// Two kernels, in stream order:
 //   1. prep (CUDA cores, one warp per (b, KV head, row q)): Delta for every
 //      query head of the group; the whole backward of the diagonal suffix keys
 //      (q < T, blocks j = 1..k: one key per query, so dK_j / dV_j row q is owned
 //      by this warp and written directly); dq initialised with the suffix part;
 //      dK_0 / dV_0 zeroed for the causal kernel's accumulation.
-//   2. dq (tcgen05, one CTA per 128-row query tile of a head, like the
-//      forward): S = Q K^T and dP = dO V^T in TMEM, dS written back into TMEM
-//      as bf16, dQ += dS K (A operand read from TMEM); dq += scale dQ.
-//   3. dkdv (tcgen05, one CTA per 128-row key tile of a query head): S^T =
-//      K Q^T and dP^T = V dO^T in TMEM, P^T and dS^T written back into TMEM as
-//      bf16, dV += P^T dO and dK += dS^T Q accumulate in TMEM over the query
-//      tiles; the group's query heads are summed with fp32 atomics.
-// In both tcgen05 kernels 8 compute warps share the element-wise phase: warps
-// w and w+4 read the same TMEM lane quarter and split its columns in halves.
-// dq is written once per row by exactly one CTA (deterministic); dK_0 / dV_0
-// sum G partials per element in arrival order.
+//   2. causal (tcgen05, one CTA per 128-row key tile of a query head, looping
+//      over the query tiles that see it): S^T = K Q^T and dP^T = V dO^T in
+//      TMEM; 8 compute warps form P^T (written back into TMEM as bf16) and
+//      dS^T (written to shared memory as bf16); then dV += P^T dO (A from
+//      TMEM), dK += dS^T Q and dQ = dS K (A = the same dS^T tile read
+//      MN-major, i.e. transposed) run on the tensor cores.  dV and dK stay in
+//      TMEM across the query tiles.  Each tile's dQ is staged in shared memory
+//      and added to the fp32 dq by TMA reduce-add; the final dK / dV of the
+//      key tile are reduce-added the same way into dK_0 / dV_0, summing the
+//      group's query heads.
+// Every causal score entry costs 5 tensor-core products (the useful 10*D
+// flops); dq, dK_0 and dV_0 receive their partial sums in arrival order.
 #include "../../include/stt.h"
 #include "attn_common.cuh"
 
@@ -32,6 +33,7 @@ namespace {
 
 constexpr int kThreads = 320;   // warps 0-7 compute, 8 TMA, 9 MMA
 constexpr int kCompute = 256;
+constexpr int kComputeWarps = kCompute / 32;  // barriers count one arrival per warp
 constexpr int kWarpTma = 8, kWarpMma = 9;
 
 struct BwdParams {
@@ -77,6 +79,11 @@ __device__ __forceinline__ void store_f32(float* p, const float (&v)[E]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   else
     *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+}
+
+// Row r, 16-byte chunk w of a swizzled [128 rows x 128 bytes] staging block.
+__device__ __forceinline__ uint32_t swz128(int r, int w) {
+  return (uint32_t)(r * 128 + ((w ^ (r & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ prep --
@@ -176,253 +183,47 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
   }
 }
 
-// TMEM columns shared by both tcgen05 kernels.
+// ---------------------------------------------------------------- causal --
+// TMEM columns: S^T (P^T is written back into it), dP^T (reused for this
+// tile's dQ), dV, dK.  Column half h of P^T lives in S^T columns
+// [64h, 64h + 32), inside the S^T columns its own warps read, so the write-back
+// needs no barrier between the two halves.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
-
-// -------------------------------------------------------------------- dq --
-template <int D>
-struct DqSmem {
-  static constexpr int kTileB = kTile * D * 2;
-  static constexpr int kStages = 2;
-  static constexpr int q = 0;
-  static constexpr int dO = kTileB;
-  static constexpr int k0 = 2 * kTileB;
-  static constexpr int v0 = 2 * kTileB + kStages * kTileB;
-  static constexpr int total = 2 * kTileB + 2 * kStages * kTileB;
-  static constexpr int alloc = total + 1024;
-};
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV) {
-  using L = DqSmem<D>;
-  constexpr int NS = L::kStages;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_qdo, bar_kv_full[NS], bar_kv_empty[NS], bar_sdp_full, bar_ds_ready,
-      bar_dq_done, bar_drain, bar_grp;
-  __shared__ uint32_t tmem_base;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nb = P.H * P.B;
-  const int t = P.n_t - 1 - (int)(blockIdx.x / nb);
-  const int bh = (int)(blockIdx.x % nb);
-  const int b = bh / P.H, h = bh % P.H, hk = h / P.G;
-  const int q0 = t * kTile;
-  const int T = P.T[b];
-  const int n_kv = causal_kv_tiles(q0, T);
-
-  if (tid == 0) {
-    mbar_init(&bar_qdo, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bar_kv_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
-    }
-    mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_ds_ready, kCompute);
-    mbar_init(&bar_dq_done, 1);
-    mbar_init(&bar_drain, 1);
-    mbar_init(&bar_grp, kCompute);
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(&tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base;
-
-  if (warp == kWarpTma) {
-    if (lane == 0 && n_kv > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmDO);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int bhk = b * P.H_kv + hk;
-      mbar_arrive_expect_tx(&bar_qdo, 2 * L::kTileB);
-      for (int cb = 0; cb < D / kColBlock; ++cb) {
-        tma_load_3d(smem + L::q + cb * kTile * 128, &tmQ, &bar_qdo, cb * kColBlock, q0, bh);
-        tma_load_3d(smem + L::dO + cb * kTile * 128, &tmDO, &bar_qdo, cb * kColBlock, q0, bh);
-      }
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % NS;
-        if (j >= NS && !mbar_wait(&bar_kv_empty[st], ((uint32_t)(j / NS) & 1u) ^ 1u, STT_DEVERR_BWD_WAIT))
-          break;
-        mbar_arrive_expect_tx(&bar_kv_full[st], 2 * L::kTileB);
-        for (int cb = 0; cb < D / kColBlock; ++cb) {
-          tma_load_3d(smem + L::k0 + st * L::kTileB + cb * kTile * 128, &tmK, &bar_kv_full[st],
-                      cb * kColBlock, j * kTile, bhk);
-          tma_load_3d(smem + L::v0 + st * L::kTileB + cb * kTile * 128, &tmV, &bar_kv_full[st],
-                      cb * kColBlock, j * kTile, bhk);
-        }
-        ++issued;
-      }
-      if (issued < n_kv) {
-        mbar_wait(&bar_qdo, 0, STT_DEVERR_BWD_WAIT);
-        for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-          mbar_wait(&bar_kv_full[j % NS], (uint32_t)(j / NS) & 1u, STT_DEVERR_BWD_WAIT);
-      }
-    }
-  } else if (warp == kWarpMma) {
-    if (lane == 0 && n_kv > 0) {
-      const uint32_t idSS = idesc_bf16(128, kTile, false, false);
-      const uint32_t idDQ = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(smem + L::q), aDO = smem_u32(smem + L::dO);
-      bool ok = mbar_wait(&bar_qdo, 0, STT_DEVERR_BWD_WAIT);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % NS;
-        ok = mbar_wait(&bar_kv_full[st], (uint32_t)(j / NS) & 1u, STT_DEVERR_BWD_WAIT);
-        if (ok && j > 0) ok = mbar_wait(&bar_dq_done, (uint32_t)(j - 1) & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t aK = smem_u32(smem + L::k0 + st * L::kTileB);
-        const uint32_t aV = smem_u32(smem + L::v0 + st * L::kTileB);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
-                       idSS, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aDO + off, 16, 1024),
-                       sdesc_sw128(aV + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&bar_sdp_full);
-        ok = mbar_wait(&bar_ds_ready, (uint32_t)j & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ += dS K: A = dS (bf16 in TMEM, 8 columns per 16 keys), B = K [kv][d] MN-major.
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ts(tmem + kColAcc0, tmem + kColS + kk * 8,
-                       sdesc_sw128(aK + kk * 2048, kTile * 128, 1024), idDQ,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar_dq_done);
-        umma_commit(&bar_kv_empty[st]);
-      }
-      umma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
-    }
-  } else {
-    // Compute warps: row r = TMEM lane; `half` selects the 64-column half.
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;
-    const int qrow = q0 + r;
-    const int lim = causal_row_limit(qrow, T);
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool in_range = qrow < P.Q_LEN;
-    const size_t rq = (size_t)bh * P.Q_LEN + qrow;
-    const float lse2 = in_range ? P.lse[rq] * kLog2e : 0.f;
-    const float dlt = in_range ? P.delta[rq] : 0.f;
-    const float sl2 = P.scale_log2;
-    uint32_t grp_uses = 0;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = warp_wait(&bar_sdp_full, (uint32_t)j & 1u, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
-      tc_fence_after();
-      const int c0 = j * kTile;
-      uint32_t s[2][32], dp[2][32];
-      tmem_ld64x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColDP + half * 64, s[0],
-                  s[1], dp[0], dp[1]);
-      // Every compute thread holds its S / dP columns before dS overwrites S.
-      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
-      const bool full = (c0 + kTile - 1 <= lim) && in_range;
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int cc = half * 2 + c2;
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(s[c2][i]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(s[c2][i + 1]), sl2, -lse2));
-          if (!full) {
-            if (!(in_range && c0 + cc * 32 + i <= lim)) p0 = 0.f;
-            if (!(in_range && c0 + cc * 32 + i + 1 <= lim)) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(dp[c2][i]) - dlt);
-          const float d1 = p1 * (__uint_as_float(dp[c2][i + 1]) - dlt);
-          pk[i >> 1] = pack_bf16(d0, d1);
-        }
-        tmem_st16(tmem + lane_off + kColS + cc * 16, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar_ds_ready);
-    }
-    if (ok && n_kv > 0) {
-      ok = warp_wait(&bar_dq_done, (uint32_t)(n_kv - 1) & 1u, STT_DEVERR_BWD_WAIT);
-      tc_fence_after();
-      if (ok) {
-        float* dqrow = P.dq + rq * D;
-#pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          const int c = half * (D / 64) + c2;
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_off + kColAcc0 + c * 32, u);
-          if (in_range) {
-            float4* d4 = reinterpret_cast<float4*>(dqrow + c * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              float4 v = d4[q4];
-              v.x = fmaf(P.scale, __uint_as_float(u[4 * q4 + 0]), v.x);
-              v.y = fmaf(P.scale, __uint_as_float(u[4 * q4 + 1]), v.y);
-              v.z = fmaf(P.scale, __uint_as_float(u[4 * q4 + 2]), v.z);
-              v.w = fmaf(P.scale, __uint_as_float(u[4 * q4 + 3]), v.w);
-              d4[q4] = v;
-            }
-          }
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ------------------------------------------------------------------ dkdv --
-template <int D>
-struct DkvSmem {
-  static constexpr int kTileB = kTile * D * 2;
+struct CausalSmem {
+  static constexpr int kTileB = kTile * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kDsB = kTile * kTile * 2;
   static constexpr int kStages = 2;
   static constexpr int k = 0;
   static constexpr int v = kTileB;
   static constexpr int q0 = 2 * kTileB;
   static constexpr int do0 = 2 * kTileB + kStages * kTileB;
-  static constexpr int total = 2 * kTileB + 2 * kStages * kTileB;
+  static constexpr int ds = 2 * kTileB + 2 * kStages * kTileB;
+  static constexpr int total = ds + kDsB;
   static constexpr int alloc = total + 1024;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams P, const __grid_constant__ CUtensorMap tmQ,
-                         const __grid_constant__ CUtensorMap tmDO,
-                         const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV) {
-  using L = DkvSmem<D>;
+    attn_bwd_causal_kernel(const __grid_constant__ BwdParams P,
+                           const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmDO,
+                           const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV,
+                           const __grid_constant__ CUtensorMap tmDQ,
+                           const __grid_constant__ CUtensorMap tmDK,
+                           const __grid_constant__ CUtensorMap tmDV) {
+  using L = CausalSmem<D>;
   constexpr int NS = L::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_kv, bar_qdo_full[NS], bar_qdo_empty[NS], bar_sdp_full, bar_pds_ready,
-      bar_acc_done, bar_drain, bar_grp;
+      bar_acc_done, bar_dq_free, bar_stage_free, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_stat[2][2][kTile];  // [slot][lse2 | delta][query]
+  __shared__ __align__(16) float s_stat[2][kTile];  // [lse2 | Delta][query] of the current tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -441,10 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_qdo_empty[s], 1);
     }
     mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_pds_ready, kCompute);
+    mbar_init(&bar_pds_ready, kComputeWarps);
     mbar_init(&bar_acc_done, 1);
+    mbar_init(&bar_dq_free, kComputeWarps);
+    mbar_init(&bar_stage_free, 1);
     mbar_init(&bar_drain, 1);
-    mbar_init(&bar_grp, kCompute);
+    mbar_init(&bar_grp, kComputeWarps);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -457,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base;
 
   if (warp == kWarpTma) {
+    // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_q > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
@@ -472,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_q; ++i) {
         const int st = i % NS;
         const int tq = (t_first + i) * kTile;
-        if (i >= NS && !mbar_wait(&bar_qdo_empty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, STT_DEVERR_BWD_WAIT))
+        // The stage is released once its tile's MMAs are done and the dQ
+        // staging that borrows the dO buffer has been read by TMA.
+        if (i >= NS &&
+            !mbar_wait(&bar_qdo_empty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, STT_DEVERR_BWD_WAIT))
           break;
         mbar_arrive_expect_tx(&bar_qdo_full[st], 2 * L::kTileB);
         for (int cb = 0; cb < D / kColBlock; ++cb) {
@@ -484,21 +291,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
       }
       if (issued < n_q) {
+        // Gave up: let every copy already issued land before the CTA exits.
         mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
         for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
           mbar_wait(&bar_qdo_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
       }
     }
   } else if (warp == kWarpMma) {
+    // -------------------------------------------------------- MMA issuer --
     if (lane == 0 && n_q > 0) {
-      const uint32_t idSS = idesc_bf16(128, kTile, false, false);
-      const uint32_t idACC = idesc_bf16(128, D, false, true);
+      const uint32_t idSS = idesc_bf16(128, kTile, false, false);  // S^T, dP^T
+      const uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK (B MN-major)
+      const uint32_t idQ = idesc_bf16(128, D, true, true);         // dQ (A, B MN-major)
       const uint32_t aK = smem_u32(smem + L::k), aV = smem_u32(smem + L::v);
+      const uint32_t aDS = smem_u32(smem + L::ds);
       bool ok = mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % NS;
+        const uint32_t par = (uint32_t)(i - 1) & 1u;
         ok = mbar_wait(&bar_qdo_full[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
-        if (ok && i > 0) ok = mbar_wait(&bar_acc_done, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+        // P^T and dS^T of the previous tile consumed by its MMAs.
+        if (ok && i > 0) ok = mbar_wait(&bar_acc_done, par, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         tc_fence_after();
         const uint32_t aQ = smem_u32(smem + L::q0 + st * L::kTileB);
@@ -506,9 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024),
-                       idSS, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024),
+                       sdesc_sw128(aQ + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
         }
+        // The previous tile's dQ has been read out of the dP^T columns.
+        if (i > 0 && !mbar_wait(&bar_dq_free, par, STT_DEVERR_BWD_WAIT)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
@@ -519,32 +338,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bar_pds_ready, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q: A from TMEM (query index = K dim), B MN-major.
+        // dV += P^T dO: A = P^T in TMEM (8 columns per 16 queries; queries
+        // 64h.. live at column 64h), B = dO MN-major.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ts(tmem + kColAcc0, tmem + kColS + kk * 8,
-                       sdesc_sw128(aDO + kk * 2048, kTile * 128, 1024), idACC,
+          umma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                       sdesc_sw128(aDO + kk * 2048, kTile * 128, 1024), idKV,
                        (i > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q: A = dS^T in smem (K-major over queries), B = Q MN-major.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ts(tmem + kColAcc1, tmem + kColDP + kk * 8,
-                       sdesc_sw128(aQ + kk * 2048, kTile * 128, 1024), idACC,
+          umma_bf16_ss(tmem + kColDK,
+                       sdesc_sw128(aDS + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024),
+                       sdesc_sw128(aQ + kk * 2048, kTile * 128, 1024), idKV,
                        (i > 0 || kk > 0) ? 1u : 0u);
+        // dQ = dS K: A = the same dS^T tile read MN-major (rows = keys = K dim),
+        // B = K MN-major; into the dP^T columns.
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aDS + kk * 2048, kTile * 128, 1024),
+                       sdesc_sw128(aK + kk * 2048, kTile * 128, 1024), idQ, kk > 0 ? 1u : 0u);
         umma_commit(&bar_acc_done);
-        umma_commit(&bar_qdo_empty[st]);
       }
+      // Every MMA issued by this thread is complete before TMEM is released.
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
     }
   } else {
-    // Compute warps: key row = TMEM lane; `half` selects the 64-query half.
+    // ------------------------------------------------------ compute warps --
+    // Row r of the TMEM lane quarter is key row c0 + r for S^T / dP^T / dV / dK
+    // and query row tq0 + r for dQ; `half` selects the 64-column half.
     const int quarter = warp & 3, half = warp >> 2;
-    const int kv = c0 + quarter * 32 + lane;
+    const int r = quarter * 32 + lane;
+    const int kv = c0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = P.scale_log2;
     const bool kv_live = kv < T;  // T <= Q_LEN, so also kv < Q_LEN
-    // Thread tid stages one statistic of one query of the tile: lse2 (tid < 128)
-    // or Delta (tid >= 128) of query tq0 + (tid & 127); prefetched a tile ahead.
+    unsigned char* sDS = smem + L::ds;
+    // Thread tid stages one statistic of one query of a tile: lse2 (tid < 128)
+    // or Delta (tid >= 128) of query tq0 + (tid & 127).
     const int st_which = tid >> 7, st_idx = tid & 127;
     auto fetch_stat = [&](int i) -> float {
       const int qq = (t_first + i) * kTile + st_idx;
@@ -552,84 +384,161 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t rq = (size_t)bh * P.Q_LEN + qq;
       return st_which == 0 ? P.lse[rq] * kLog2e : P.delta[rq];
     };
-    float stat_next = n_q > 0 ? fetch_stat(0) : 0.f;
     uint32_t grp_uses = 0;
     bool ok = true;
-    for (int i = 0; i < n_q; ++i) {
-      const int tq0 = (t_first + i) * kTile;
-      const int slot = i & 1;
-      s_stat[slot][st_which][st_idx] = stat_next;
-      if (i + 1 < n_q) stat_next = fetch_stat(i + 1);
+    float stat_next = 0.f;
+    if (n_q > 0) {
+      s_stat[st_which][st_idx] = fetch_stat(0);
+      if (n_q > 1) stat_next = fetch_stat(1);
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
+    }
+    for (int i = 0; ok && i < n_q; ++i) {
+      const int st = i % NS;
+      const int tq0 = (t_first + i) * kTile;
+      const int qh = tq0 + half * 64;  // first query of this thread's half
+      // Every compute thread finished the previous tile: this tile's
+      // statistics are in shared memory.
+      if (i > 0) {
+        ok = warp_wait(&bar_dq_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+        if (!ok) break;
+      }
       ok = warp_wait(&bar_sdp_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[2][32], dp[2][32];
-      tmem_ld64x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColDP + half * 64, s[0],
-                  s[1], dp[0], dp[1]);
-      // Every compute thread holds its S^T / dP^T columns before they are overwritten.
-      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
-      const bool full = kv_live && kv <= tq0 && tq0 + kTile <= P.Q_LEN;
-      const float* lse_s = s_stat[slot][0];
-      const float* dl_s = s_stat[slot][1];
+      const bool full = kv_live && kv <= qh && qh + 64 <= P.Q_LEN;
+      const float* lse_s = s_stat[0] + half * 64;
+      const float* dl_s = s_stat[1] + half * 64;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        const int cc = half * 2 + c2;
-        uint32_t pp[16], dd[16];
+        uint32_t s[32], dp[32], pp[16], dd[16];
+        tmem_ld32x2(tmem + lane_off + kColS + half * 64 + c2 * 32,
+                    tmem + lane_off + kColDP + half * 64 + c2 * 32, s, dp);
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int ql = cc * 32 + x;
-          const int qa = tq0 + ql;
-          float p0 = ex2(fmaf(__uint_as_float(s[c2][x]), sl2, -lse_s[ql]));
-          float p1 = ex2(fmaf(__uint_as_float(s[c2][x + 1]), sl2, -lse_s[ql + 1]));
-          if (!full) {
-            if (!(kv_live && kv <= qa && qa < P.Q_LEN)) p0 = 0.f;
-            if (!(kv_live && kv <= qa + 1 && qa + 1 < P.Q_LEN)) p1 = 0.f;
+        for (int x4 = 0; x4 < 32; x4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
+          const float4 d4 = *reinterpret_cast<const float4*>(dl_s + c2 * 32 + x4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], sv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pv[e] = ex2(fmaf(__uint_as_float(s[x4 + e]), sl2, -lv[e]));
+            if (!full) {
+              const int qa = qh + c2 * 32 + x4 + e;
+              if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv[e] = 0.f;
+            }
+            sv[e] = pv[e] * (__uint_as_float(dp[x4 + e]) - dv[e]);
           }
-          const float d0 = p0 * (__uint_as_float(dp[c2][x]) - dl_s[ql]);
-          const float d1 = p1 * (__uint_as_float(dp[c2][x + 1]) - dl_s[ql + 1]);
-          pp[x >> 1] = pack_bf16(p0, p1);
-          dd[x >> 1] = pack_bf16(d0, d1);
+          pp[x4 >> 1] = pack_bf16(pv[0], pv[1]);
+          pp[(x4 >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+          dd[x4 >> 1] = pack_bf16(sv[0], sv[1]);
+          dd[(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
         }
-        tmem_st16(tmem + lane_off + kColS + cc * 16, pp);
-        tmem_st16(tmem + lane_off + kColDP + cc * 16, dd);
+        // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
+        tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
+        if (c2 == 0 && i > 0) {
+          // The dS^T buffer (and the previous tile's dO buffer) hold the
+          // previous tile's dQ staging until TMA has read them.
+          if (tid == 0) {
+            bulk_wait_group_read0();
+            mbar_arrive(&bar_stage_free);
+            mbar_arrive(&bar_qdo_empty[(i - 1) % NS]);
+          }
+          ok = warp_wait(&bar_stage_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+        }
+        // dS^T row kv, queries [qh + 32 c2, +32) -> swizzled [key][query] tile
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          *reinterpret_cast<uint4*>(sDS + swz_chunk_offset(r, half * 8 + c2 * 4 + w, kTile)) =
+              make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
       }
+      if (!ok) break;
       tmem_st_wait();
+      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_pds_ready);
+      warp_arrive(&bar_pds_ready);
+
+      // Statistics of the next tile, once every warp is done with this one's.
+      ok = warp_wait(&bar_pds_ready, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      if (i + 1 < n_q) {
+        s_stat[st_which][st_idx] = stat_next;
+        if (i + 2 < n_q) stat_next = fetch_stat(i + 2);
+      }
+
+      // This tile's dQ (rows = queries tq0 + r), staged as swizzled [128 x 32]
+      // fp32 blocks: the 64 columns of half h go to the dS^T buffer (pass 0) and
+      // the dO buffer of this tile (pass 1), both free once the MMAs are done.
+      ok = warp_wait(&bar_acc_done, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      tc_fence_after();
+      unsigned char* stage[2] = {sDS, smem + L::do0 + st * L::kTileB};
+#pragma unroll
+      for (int pss = 0; pss < D / 64; ++pss) {
+        const int cc = half * (D / 64) + pss;  // this thread's 32-column chunk
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + kColDP + cc * 32, u);
+        unsigned char* blk = stage[pss] + half * (kTile * 128);
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+          *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
+              P.scale * __uint_as_float(u[4 * w]), P.scale * __uint_as_float(u[4 * w + 1]),
+              P.scale * __uint_as_float(u[4 * w + 2]), P.scale * __uint_as_float(u[4 * w + 3]));
+      }
+      // dQ is out of TMEM: the MMA warp may overwrite the dP^T columns.
+      tc_fence_before();
+      warp_arrive(&bar_dq_free);
+      fence_proxy_async_smem();
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      if (tid == 0) {
+#pragma unroll
+        for (int pss = 0; pss < D / 64; ++pss) {
+          tma_reduce_add_3d(&tmDQ, stage[pss], pss * 32, tq0, bh);
+          tma_reduce_add_3d(&tmDQ, stage[pss] + kTile * 128, (D / 64 + pss) * 32, tq0, bh);
+        }
+        bulk_commit_group();
+      }
     }
     if (ok && n_q > 0) {
-      ok = warp_wait(&bar_acc_done, (uint32_t)(n_q - 1) & 1u, STT_DEVERR_BWD_WAIT);
-      tc_fence_after();
-      if (ok) {
-        const size_t off = ((size_t)(b * P.H_kv + hk) * P.Q_LEN + kv) * D;
-        float* dkr = P.dkb[0] + off;
-        float* dvr = P.dvb[0] + off;
+      // dV and dK of this key tile into the block-0 gradients, summed over the
+      // group's query heads: K, V and the Q stages are free now, so all D/32
+      // chunks of both are staged at once (below the dO stages, which may
+      // still be read by the last dQ reduction) and reduce-added by TMA (rows
+      // kv >= T hold zeros; rows past Q_LEN are clipped).
 #pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          const int cc = half * (D / 64) + c2;
-          uint32_t uv[32], uk[32];
-          tmem_ld32x2(tmem + lane_off + kColAcc0 + cc * 32, tmem + lane_off + kColAcc1 + cc * 32,
-                      uv, uk);
-          if (kv_live) {
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        const int cc = half * (D / 64) + c2;
+        uint32_t uv[32], uk[32];
+        tmem_ld32x2(tmem + lane_off + kColDV + cc * 32, tmem + lane_off + kColDK + cc * 32, uv, uk);
+        unsigned char* bv = smem + cc * (kTile * 128);
+        unsigned char* bk = smem + (D / 32 + cc) * (kTile * 128);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              atomicAdd(reinterpret_cast<float4*>(dvr + cc * 32) + q4,
-                        make_float4(__uint_as_float(uv[4 * q4]), __uint_as_float(uv[4 * q4 + 1]),
-                                    __uint_as_float(uv[4 * q4 + 2]), __uint_as_float(uv[4 * q4 + 3])));
-              atomicAdd(reinterpret_cast<float4*>(dkr + cc * 32) + q4,
-                        make_float4(P.scale * __uint_as_float(uk[4 * q4]),
-                                    P.scale * __uint_as_float(uk[4 * q4 + 1]),
-                                    P.scale * __uint_as_float(uk[4 * q4 + 2]),
-                                    P.scale * __uint_as_float(uk[4 * q4 + 3])));
-            }
-          }
+        for (int w = 0; w < 8; ++w) {
+          const uint32_t o = swz128(r, w);
+          *reinterpret_cast<float4*>(bv + o) =
+              make_float4(__uint_as_float(uv[4 * w]), __uint_as_float(uv[4 * w + 1]),
+                          __uint_as_float(uv[4 * w + 2]), __uint_as_float(uv[4 * w + 3]));
+          *reinterpret_cast<float4*>(bk + o) = make_float4(
+              P.scale * __uint_as_float(uk[4 * w]), P.scale * __uint_as_float(uk[4 * w + 1]),
+              P.scale * __uint_as_float(uk[4 * w + 2]), P.scale * __uint_as_float(uk[4 * w + 3]));
         }
       }
+      fence_proxy_async_smem();
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
+      if (ok && tid == 0) {
+        const int bhk = b * P.H_kv + hk;
+        for (int cc = 0; cc < D / 32; ++cc) {
+          tma_reduce_add_3d(&tmDV, smem + cc * (kTile * 128), cc * 32, c0, bhk);
+          tma_reduce_add_3d(&tmDK, smem + (D / 32 + cc) * (kTile * 128), cc * 32, c0, bhk);
+        }
+        bulk_commit_group();
+      }
     }
+    // The issuing thread waits for its reductions before the CTA's shared memory goes away.
+    if (tid == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -638,6 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
+static_assert(2 * 128 / 32 * 16384 <= 4 * 32768, "dK/dV staging must stay below the dO stages");
 
 template <int D, int GM>
 void launch_prep(const BwdParams& P, long long blocks, cudaStream_t s) {
@@ -678,6 +589,12 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
     return e;
   if ((e = encode_tile_map(&tmV, a.v_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
+  CUtensorMap tmDQ, tmDK, tmDV;
+  if ((e = encode_f32_map(&tmDQ, g.dq, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
+  if ((e = encode_f32_map(&tmDK, g.dk_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
+    return e;
+  if ((e = encode_f32_map(&tmDV, g.dv_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
+    return e;
 
   const long long rows = (long long)a.B * a.H_kv * a.Q_LEN;
   long long blocks = (rows + 7) / 8;
@@ -695,19 +612,12 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const unsigned grid = (unsigned)(P.n_t * a.H * a.B);
-  e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DqSmem<D>::alloc);
+  e = cudaFuncSetAttribute(attn_bwd_causal_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           CausalSmem<D>::alloc);
   if (e != cudaSuccess) return e;
-  prof_before(s, STT_KERNEL_ATTN_BWD_DQ);
-  attn_bwd_dq_kernel<D><<<grid, kThreads, DqSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV);
-  prof_after(s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DkvSmem<D>::alloc);
-  if (e != cudaSuccess) return e;
-  prof_before(s, STT_KERNEL_ATTN_BWD_DKDV);
-  attn_bwd_dkdv_kernel<D><<<grid, kThreads, DkvSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV);
+  prof_before(s, STT_KERNEL_ATTN_BWD_CAUSAL);
+  attn_bwd_causal_kernel<D><<<grid, kThreads, CausalSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV,
+                                                                        tmDQ, tmDK, tmDV);
   prof_after(s);
   return cudaGetLastError();
 }

@@ -55,18 +55,43 @@ inline cudaError_t encode_tile_map(CUtensorMap* map, const void* base, int D, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// fp32 [outer][rows][D] tensor map with a 32 x box_rows box (128-byte rows) and
+// 128-byte swizzle: the staging layout used for reduce-add of gradients.
+inline cudaError_t encode_f32_map(CUtensorMap* map, const void* base, int D, int rows, int outer,
+                                  int box_rows) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * 4 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Warp-uniform bounded wait: every lane waits, the warp agrees on success.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t site) {
   const bool ok = mbar_wait(bar, parity, site);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
-// Bounded barrier among the threads counted by `bar` (an mbarrier initialised
-// with that count).  Unlike a named hardware barrier it cannot deadlock when
-// some thread gave up on an earlier bounded wait: the others time out too.
+// One arrival per warp on `bar` (an mbarrier counting warps): the warp's lanes
+// first meet at __syncwarp, which orders their prior shared-memory and (after
+// their own tcgen05 fences) tensor-memory accesses before lane 0's release
+// arrive.  Every lane of the warp must call it.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Bounded barrier among the warps counted by `bar` (an mbarrier initialised
+// with that many warps).  Unlike a named hardware barrier it cannot deadlock
+// when some warp gave up on an earlier bounded wait: the others time out too.
 // `uses` counts this thread's completed phases (same sequence in every thread).
 __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& uses, uint32_t site) {
-  mbar_arrive(bar);
+  warp_arrive(bar);
   const bool ok = warp_wait(bar, uses & 1u, site);
   ++uses;
   return ok;

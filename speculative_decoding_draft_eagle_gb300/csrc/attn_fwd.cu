@@ -35,6 +35,7 @@ namespace {
 constexpr int kStages = 2;
 constexpr int kThreads = 320;
 constexpr int kSoftmax = 256;
+constexpr int kSoftmaxWarps = kSoftmax / 32;  // barriers count one arrival per warp
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
 
@@ -125,16 +126,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_k_empty[s], 1);
       mbar_init(&bar_v_empty[s], 1);
       mbar_init(&bar_sfx_full[s], 1);
-      mbar_init(&bar_sfx_empty[s], kSoftmax);
+      mbar_init(&bar_sfx_empty[s], kSoftmaxWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_free[s], kSoftmax);
+      mbar_init(&bar_s_free[s], kSoftmaxWarps);
     }
-    mbar_init(&bar_p_full, kSoftmax);
+    mbar_init(&bar_p_full, kSoftmaxWarps);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
-    mbar_init(&bar_grp, kSoftmax);
+    mbar_init(&bar_grp, kSoftmaxWarps);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32x2(tmem + lane_off + kColS0 + sb * kTile + half * 64,
                   tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
       tc_fence_before();
-      mbar_arrive(&bar_s_free[sb]);
+      warp_arrive(&bar_s_free[sb]);
 
       const int cbase = j * kTile + half * 64;
       float mt = -INFINITY;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar_p_full);
+      warp_arrive(&bar_p_full);
     }
     if (ok && n_kv > 0) {
       ok = warp_wait(&bar_o_done, (uint32_t)(n_kv - 1) & 1u, STT_DEVERR_FWD_WAIT);
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[c * 8 + 7] = fmaf(pj, bf16hi(x.w), o[c * 8 + 7]);
         }
       }
-      mbar_arrive(&bar_sfx_empty[st]);
+      warp_arrive(&bar_sfx_empty[st]);
     }
 
     // ----------------------------------------------------------- epilogue --

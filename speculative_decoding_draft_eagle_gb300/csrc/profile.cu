@@ -97,8 +97,7 @@ const char* stt_kernel_name(int kernel_id) {
     case STT_KERNEL_SOFT_CE_LOSS_SUM: return "soft_ce_loss_sum";
     case STT_KERNEL_ATTN_FWD: return "attn_fwd";
     case STT_KERNEL_ATTN_BWD_PREP: return "attn_bwd_prep";
-    case STT_KERNEL_ATTN_BWD_DQ: return "attn_bwd_dq";
-    case STT_KERNEL_ATTN_BWD_DKDV: return "attn_bwd_dkdv";
+    case STT_KERNEL_ATTN_BWD_CAUSAL: return "attn_bwd_causal";
     default: return "unknown";
   }
 }
