@@ -409,9 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = kv_live && kv <= qh && qh + 64 <= P.Q_LEN;
       const float* lse_s = s_stat[0] + half * 64;
       const float* dl_s = s_stat[1] + half * 64;
+      uint32_t dd[2][16];  // dS^T of both chunks, stored once the staging buffer is free
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t s[32], dp[32], pp[16], dd[16];
+        uint32_t s[32], dp[32], pp[16];
         tmem_ld32x2(tmem + lane_off + kColS + half * 64 + c2 * 32,
                     tmem + lane_off + kColDP + half * 64 + c2 * 32, s, dp);
 #pragma unroll
@@ -432,29 +433,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pp[x4 >> 1] = pack_bf16(pv[0], pv[1]);
           pp[(x4 >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-          dd[x4 >> 1] = pack_bf16(sv[0], sv[1]);
-          dd[(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
+          dd[c2][x4 >> 1] = pack_bf16(sv[0], sv[1]);
+          dd[c2][(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
         }
         // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
         tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
-        if (c2 == 0 && i > 0) {
-          // The dS^T buffer (and the previous tile's dO buffer) hold the
-          // previous tile's dQ staging until TMA has read them.
-          if (tid == 0) {
-            bulk_wait_group_read0();
-            mbar_arrive(&bar_stage_free);
-            mbar_arrive(&bar_qdo_empty[(i - 1) % NS]);
-          }
-          ok = warp_wait(&bar_stage_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
-          if (!ok) break;
+      }
+      if (i > 0) {
+        // The dS^T buffer (and the previous tile's dO buffer) hold the
+        // previous tile's dQ staging until TMA has read them.
+        if (tid == 0) {
+          bulk_wait_group_read0();
+          mbar_arrive(&bar_stage_free);
+          mbar_arrive(&bar_qdo_empty[(i - 1) % NS]);
         }
-        // dS^T row kv, queries [qh + 32 c2, +32) -> swizzled [key][query] tile
+        ok = warp_wait(&bar_stage_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+        if (!ok) break;
+      }
+      // dS^T row kv, queries [qh, qh + 64) -> swizzled [key][query] tile
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           *reinterpret_cast<uint4*>(sDS + swz_chunk_offset(r, half * 8 + c2 * 4 + w, kTile)) =
-              make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
-      }
-      if (!ok) break;
+              make_uint4(dd[c2][4 * w], dd[c2][4 * w + 1], dd[c2][4 * w + 2], dd[c2][4 * w + 3]);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
