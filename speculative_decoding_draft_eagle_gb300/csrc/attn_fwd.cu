@@ -19,13 +19,15 @@
 //   warps 0-7  softmax: warps w and w+4 own the 32 query rows of TMEM lane
 //              quarter w%4 and split the 128 key columns (and O's D columns)
 //              in halves; the row max is exchanged through shared memory.
-//              They load S from TMEM, mask, exponentiate, write P (bf16) to
-//              shared memory, rescale O in TMEM when the running max grows by
-//              more than 2^8, and finish with the suffix keys and O / lse.
+//              They load S from TMEM, mask, exponentiate, write P (bf16) back
+//              over their own S columns in TMEM, rescale O in TMEM when the
+//              running max grows by more than 2^8, and finish with the suffix
+//              keys and O / lse.
 //   warp 8     TMA producer (one lane): Q once, then K/V tiles (2 stages),
 //              then the suffix K_j / V_j tiles through the same buffers.
 //   warp 9     MMA issuer (one lane): S(j) into one of two TMEM buffers, then
-//              O += P(j-1) V(j-1), so S(j+1) overlaps the softmax of tile j.
+//              O += P(j-1) V(j-1) with P read from TMEM, so S(j+1) overlaps the
+//              softmax of tile j.
 #include "../../include/stt.h"
 #include "attn_common.cuh"
 
@@ -57,16 +59,15 @@ template <int D>
 struct FwdSmem {
   static constexpr int kQ = kTile * D * 2;
   static constexpr int kKV = kTile * D * 2;
-  static constexpr int kP = kTile * kTile * 2;
   static constexpr int q = 0;
   static constexpr int k0 = kQ;
   static constexpr int v0 = kQ + kStages * kKV;
-  static constexpr int p = kQ + 2 * kStages * kKV;
-  static constexpr int total = p + kP;
+  static constexpr int total = kQ + 2 * kStages * kKV;
   static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
 };
 
-// TMEM columns: S buffers at 0 and 128, O at 256.
+// TMEM columns: S buffers at 0 and 128 (P of column half h is written back
+// into columns [64h, 64h + 32) of its S buffer), O at 256.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256;
 
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
-      bar_v_empty[kStages], bar_s_full[2], bar_s_free[2], bar_p_full, bar_o_done, bar_drain,
+      bar_v_empty[kStages], bar_s_full[2], bar_p_full, bar_o_done, bar_drain,
       bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
@@ -128,10 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_sfx_full[s], 1);
       mbar_init(&bar_sfx_empty[s], kSoftmaxWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_free[s], kSoftmaxWarps);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_s_full[s], 1);
     mbar_init(&bar_p_full, kSoftmaxWarps);
     mbar_init(&bar_o_done, 1);
     mbar_init(&bar_drain, 1);
@@ -147,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   unsigned char* sQ = smem + L::q;
-  unsigned char* sP = smem + L::p;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer --
@@ -213,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       const uint32_t idS = idesc_bf16(128, kTile, false, false);
       const uint32_t idO = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP);
+      const uint32_t aQ = smem_u32(sQ);
       bool ok = mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
       auto issue_pv = [&](int i) -> bool {
         const int st = i % kStages;
@@ -222,11 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         tc_fence_after();
         const uint32_t aV = smem_u32(smem + L::v0 + st * L::kKV);
+        // A = P in TMEM: keys 64h.. of the tile live at column 64h of the S buffer.
+        const uint32_t aP = tmem + kColS0 + (i & 1) * kTile;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(aP + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(aV + kk * 2048, kTile * 128, 1024);
-          umma_bf16_ss(tmem + kColO, ad, bd, idO, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO,
+                       (i > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bar_o_done);
         umma_commit(&bar_v_empty[st]);
@@ -235,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n_kv; ++j) {
         const int st = j % kStages, sb = j & 1;
         ok = mbar_wait(&bar_k_full[st], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+        // S buffer sb holds P(j-2) until O += P(j-2) V(j-2) has completed.
         if (ok && j >= 2)
-          ok = mbar_wait(&bar_s_free[sb], (uint32_t)((j - 2) >> 1) & 1u, STT_DEVERR_FWD_WAIT);
+          ok = mbar_wait(&bar_o_done, (uint32_t)(j - 2) & 1u, STT_DEVERR_FWD_WAIT);
         if (!ok) break;
         tc_fence_after();
         const uint32_t aK = smem_u32(smem + L::k0 + st * L::kKV);
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; ok && j < n_kv; ++j) {
       const int sb = j & 1;
       ok = warp_wait(&bar_s_full[sb], (uint32_t)(j >> 1) & 1u, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
@@ -276,8 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t s[2][32];
       tmem_ld32x2(tmem + lane_off + kColS0 + sb * kTile + half * 64,
                   tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
-      tc_fence_before();
-      warp_arrive(&bar_s_free[sb]);
 
       const int cbase = j * kTile + half * 64;
       float mt = -INFINITY;
@@ -329,12 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       l_run += rs;
 
-      if (j > 0) {
+      // P(j) goes to its own S buffer, and O += P(j) V(j) is ordered after
+      // O += P(j-1) V(j-1) on the tensor pipe, so only a rescale of O has to
+      // wait for the previous product (its phase is the newest one possible:
+      // the next needs this tile's P).
+      if (__any_sync(0xffffffffu, rescale_o)) {
         ok = warp_wait(&bar_o_done, (uint32_t)(j - 1) & 1u, STT_DEVERR_FWD_WAIT);
         if (!ok) break;
         tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll
         for (int c2 = 0; c2 < D / 64; ++c2) {
           uint32_t o[32];
@@ -346,13 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      // P row half -> swizzled K-major tile (A operand of O += P V).
+      // P row half (bf16 pairs) over this half's own S columns: the A operand
+      // of O += P V.
+      {
+        const uint32_t pa = tmem + lane_off + kColS0 + sb * kTile + half * 64;
+        uint32_t p0[16], p1[16];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sP + swz_chunk_offset(r, half * 8 + c, kTile)) = v;
+        for (int c = 0; c < 16; ++c) {
+          p0[c] = pk[c];
+          p1[c] = pk[16 + c];
+        }
+        tmem_st16(pa, p0);
+        tmem_st16(pa + 16, p1);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bar_p_full);
     }
