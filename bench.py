@@ -340,10 +340,14 @@ def kernel_algorithmic(sh, sc, T, g):
     bpe = 2
     nq = sh.B * H * sh.Q_LEN
     nkv = sh.B * sh.H_kv * sh.Q_LEN
+    # rows with suffix keys (q < T): only they need q, K_j and V_j, j >= 1
+    vq = sum(T) * H
+    vkv = sum(T) * sh.H_kv
     prep_bytes = 0
     for k in sh.steps:
-        prep_bytes += 3 * nq * D * bpe + 4 * nq + 4 * nq          # q, O, dO; lse; Delta
-        prep_bytes += 2 * k * nkv * D * bpe                          # K_j, V_j, j >= 1
+        prep_bytes += 2 * nq * D * bpe + 4 * nq + 4 * nq             # O, dO; lse; Delta
+        prep_bytes += (vq * D * bpe if k > 0 else 0)                 # q
+        prep_bytes += 2 * k * vkv * D * bpe                          # K_j, V_j, j >= 1
         prep_bytes += 4 * nq * D + 2 * (k + 1) * nkv * D * 4         # dq init; dK_j, dV_j
     return {
         "attn_fwd": (4 * D * (causal + suffix), "TFLOP/s"),

@@ -52,33 +52,75 @@ struct BwdParams {
   int T[kMaxBatch];
 };
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sum over the L lanes of an aligned lane group (L a power of two <= 32).
+template <int L>
+__device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = L / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// E consecutive bf16 values (E = 4 or 8) packed in pairs: one 8- or 16-byte access.
+template <int E>
+struct Bf16Vec {
+  uint32_t w[E / 2];
+};
+
+template <int E>
+__device__ __forceinline__ Bf16Vec<E> ldg_vec(const __nv_bfloat16* p) {
+  Bf16Vec<E> v;
+  if constexpr (E == 8) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(p));
+    v.w[0] = x.x;
+    v.w[1] = x.y;
+    v.w[2] = x.z;
+    v.w[3] = x.w;
+  } else {
+    const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
+    v.w[0] = x.x;
+    v.w[1] = x.y;
+  }
   return v;
 }
 
 template <int E>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&v)[E]) {
-  if constexpr (E == 4) {
-    const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
-    v[0] = bf16lo(x.x);
-    v[1] = bf16hi(x.x);
-    v[2] = bf16lo(x.y);
-    v[3] = bf16hi(x.y);
-  } else {
-    const uint32_t x = __ldg(reinterpret_cast<const uint32_t*>(p));
-    v[0] = bf16lo(x);
-    v[1] = bf16hi(x);
-  }
+__device__ __forceinline__ Bf16Vec<E> zero_vec() {
+  Bf16Vec<E> v;
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) v.w[i] = 0u;
+  return v;
 }
 
+// Dot product of two packed bf16 vectors (fp32 accumulate).
 template <int E>
-__device__ __forceinline__ void store_f32(float* p, const float (&v)[E]) {
-  if constexpr (E == 4)
-    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-  else
-    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+__device__ __forceinline__ float dot_vec(const Bf16Vec<E>& a, const Bf16Vec<E>& b) {
+  float x = 0.f, y = 0.f;
+#pragma unroll
+  for (int i = 0; i < E / 2; ++i) {
+    x = fmaf(bf16lo(a.w[i]), bf16lo(b.w[i]), x);
+    y = fmaf(bf16hi(a.w[i]), bf16hi(b.w[i]), y);
+  }
+  return x + y;
+}
+
+// Element e of a packed bf16 vector as fp32.
+template <int E>
+__device__ __forceinline__ float vec_at(const Bf16Vec<E>& a, int e) {
+  return (e & 1) ? bf16hi(a.w[e >> 1]) : bf16lo(a.w[e >> 1]);
+}
+
+// E fp32 values to 4E aligned bytes; `stream` marks lines nothing reads again.
+template <int E>
+__device__ __forceinline__ void store_vec(float* p, const float (&v)[E], bool stream) {
+  float4* p4 = reinterpret_cast<float4*>(p);
+#pragma unroll
+  for (int i = 0; i < E / 4; ++i) {
+    const float4 x = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    if (stream)
+      __stcs(p4 + i, x);
+    else
+      p4[i] = x;
+  }
 }
 
 // Row r, 16-byte chunk w of a swizzled [128 rows x 128 bytes] staging block.
@@ -87,53 +129,84 @@ __device__ __forceinline__ uint32_t swz128(int r, int w) {
 }
 
 // ------------------------------------------------------------------ prep --
-// GM: compile-time upper bound of the group size (the loops over heads are
-// unrolled so per-head values stay in registers); G <= GM at run time.
+// A group of L = D/E lanes owns one (b, KV head, row q); lane l of the group
+// holds elements [E l, E l + E) of every row it touches, so a warp covers 32/L
+// consecutive (contiguous) rows.  GM is the compile-time bound of the group
+// size (the loops over heads are unrolled so per-head values stay in
+// registers); G <= GM.
+// Register budget per group size: the per-head q, dO and dq values grow with
+// GM, so larger groups run fewer, fatter warps per SM.
+template <int GM>
+struct PrepShape {
+  static constexpr int E = 8;                               // 16-byte accesses
+  static constexpr int kJ = GM <= 2 ? 4 : (GM <= 4 ? 2 : 1);  // suffix blocks loaded together
+  static constexpr int kThreads = GM <= 2 ? 256 : 128;
+  static constexpr int kMinBlocks = GM <= 2 ? 2 : (GM <= 4 ? 3 : 2);
+};
+
 template <int D, int GM>
-__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
-  constexpr int E = D / 32;
+__global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBlocks)
+    attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
+  constexpr int E = PrepShape<GM>::E;
+  constexpr int kJ = PrepShape<GM>::kJ;
+  constexpr int L = D / E;     // lanes per row
+  constexpr int RPW = 32 / L;  // rows per warp
+  constexpr int kWarps = PrepShape<GM>::kThreads / 32;
+  using V = Bf16Vec<E>;
   const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * 8;
+  const int sub = lane / L, li = lane % L;
   const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
+  const long long stride = (long long)gridDim.x * kWarps * RPW;
   const int G = P.G;
-  for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += warps) {
-    const int q = (int)(row % P.Q_LEN);
-    const int bhk = (int)(row / P.Q_LEN);
+  for (long long base = ((long long)blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW; base < rows;
+       base += stride) {
+    // Every lane stays in the loop body (the group sums shuffle across the
+    // warp); lanes past the last row only skip their memory accesses.
+    const long long row = base + sub;
+    const bool live = row < rows;
+    const int q = live ? (int)(row % P.Q_LEN) : 0;
+    const int bhk = live ? (int)(row / P.Q_LEN) : 0;
     const int b = bhk / P.H_kv, hk = bhk % P.H_kv;
-    const bool valid = q < P.T[b];
-    const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + lane * E;
-    float qv[GM][E], dov[GM][E], dq[GM][E], lse2[GM], dl[GM];
+    const bool valid = live && q < P.T[b];  // rows with suffix keys
+    const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + li * E;
+
+    V qv[GM], dov[GM];
+    float dq[GM][E], lse2[GM], dl[GM];
+    {
+      V ov[GM];
 #pragma unroll
-    for (int i = 0; i < GM; ++i) {
-      if (i < G) {
-        const size_t rq = (size_t)(b * P.H + hk * G + i) * P.Q_LEN + q;
-        const size_t off = rq * D + lane * E;
-        float ov[E];
-        load_bf16<E>(P.dout + off, dov[i]);
-        load_bf16<E>(P.out + off, ov);
-        load_bf16<E>(P.q + off, qv[i]);
-        float d = 0.f;
+      for (int i = 0; i < GM; ++i) {
+        qv[i] = dov[i] = ov[i] = zero_vec<E>();
+        lse2[i] = 0.f;
+        if (i < G && live) {
+          const size_t rq = (size_t)(b * P.H + hk * G + i) * P.Q_LEN + q;
+          const size_t off = rq * D + li * E;
+          dov[i] = ldg_vec<E>(P.dout + off);
+          ov[i] = ldg_vec<E>(P.out + off);
+          if (valid && P.k > 0) qv[i] = ldg_vec<E>(P.q + off);
+          lse2[i] = P.lse[rq] * kLog2e;
+        }
+      }
 #pragma unroll
-        for (int e = 0; e < E; ++e) d = fmaf(dov[i][e], ov[e], d);
-        dl[i] = warp_sum(d);
-        lse2[i] = P.lse[rq] * kLog2e;
-        if (lane == 0) P.delta[rq] = dl[i];
+      for (int i = 0; i < GM; ++i) {
+        dl[i] = 0.f;
+        if (i < G) {
+          dl[i] = group_sum<L>(dot_vec<E>(dov[i], ov[i]));
+          if (live && li == 0) P.delta[(size_t)(b * P.H + hk * G + i) * P.Q_LEN + q] = dl[i];
+        }
 #pragma unroll
         for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
       }
     }
-    // Blocks are taken kJ at a time with all their row loads issued up front, so
-    // each warp keeps 2*kJ loads in flight.
-    constexpr int kJ = 4;
+    // Blocks are taken kJ at a time with all their row loads issued up front.
     for (int j0 = 1; j0 <= P.k; j0 += kJ) {
-      float kv[kJ][E], vv[kJ][E];
-      if (valid) {
+      V kv[kJ], vv[kJ];
 #pragma unroll
-        for (int u = 0; u < kJ; ++u) {
-          if (j0 + u <= P.k) {
-            load_bf16<E>(P.kb[j0 + u] + kvoff, kv[u]);
-            load_bf16<E>(P.vb[j0 + u] + kvoff, vv[u]);
-          }
+      for (int u = 0; u < kJ; ++u) {
+        kv[u] = vv[u] = zero_vec<E>();
+        if (valid && j0 + u <= P.k) {
+          kv[u] = ldg_vec<E>(P.kb[j0 + u] + kvoff);
+          vv[u] = ldg_vec<E>(P.vb[j0 + u] + kvoff);
         }
       }
 #pragma unroll
@@ -143,43 +216,39 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
         float dk[E], dv[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
-        if (valid) {
 #pragma unroll
-          for (int i = 0; i < GM; ++i) {
-            if (i < G) {
-              float s = 0.f, dp = 0.f;
+        for (int i = 0; i < GM; ++i) {
+          if (i < G) {
+            const float s = group_sum<L>(dot_vec<E>(qv[i], kv[u]));
+            const float dp = group_sum<L>(dot_vec<E>(dov[i], vv[u]));
+            // Rows without suffix keys get no contribution (their lse may be -inf).
+            const float p = valid ? ex2(s * P.scale_log2 - lse2[i]) : 0.f;
+            const float dss = p * (dp - dl[i]) * P.scale;
 #pragma unroll
-              for (int e = 0; e < E; ++e) {
-                s = fmaf(qv[i][e], kv[u][e], s);
-                dp = fmaf(dov[i][e], vv[u][e], dp);
-              }
-              s = warp_sum(s);
-              dp = warp_sum(dp);
-              const float p = ex2(s * P.scale_log2 - lse2[i]);
-              const float ds = p * (dp - dl[i]);
-              const float dss = ds * P.scale;
-#pragma unroll
-              for (int e = 0; e < E; ++e) {
-                dq[i][e] = fmaf(dss, kv[u][e], dq[i][e]);
-                dk[e] = fmaf(dss, qv[i][e], dk[e]);
-                dv[e] = fmaf(p, dov[i][e], dv[e]);
-              }
+            for (int e = 0; e < E; ++e) {
+              dq[i][e] = fmaf(dss, vec_at<E>(kv[u], e), dq[i][e]);
+              dk[e] = fmaf(dss, vec_at<E>(qv[i], e), dk[e]);
+              dv[e] = fmaf(p, vec_at<E>(dov[i], e), dv[e]);
             }
           }
         }
-        store_f32<E>(P.dkb[j] + kvoff, dk);
-        store_f32<E>(P.dvb[j] + kvoff, dv);
+        if (live) {
+          store_vec<E>(P.dkb[j] + kvoff, dk, true);
+          store_vec<E>(P.dvb[j] + kvoff, dv, true);
+        }
       }
     }
+    if (live) {
 #pragma unroll
-    for (int i = 0; i < GM; ++i)
-      if (i < G)
-        store_f32<E>(P.dq + ((size_t)(b * P.H + hk * G + i) * P.Q_LEN + q) * D + lane * E, dq[i]);
-    float z[E];
+      for (int i = 0; i < GM; ++i)
+        if (i < G)
+          store_vec<E>(P.dq + ((size_t)(b * P.H + hk * G + i) * P.Q_LEN + q) * D + li * E, dq[i], false);
+      float z[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) z[e] = 0.f;
-    store_f32<E>(P.dkb[0] + kvoff, z);
-    store_f32<E>(P.dvb[0] + kvoff, z);
+      for (int e = 0; e < E; ++e) z[e] = 0.f;
+      store_vec<E>(P.dkb[0] + kvoff, z, false);
+      store_vec<E>(P.dvb[0] + kvoff, z, false);
+    }
   }
 }
 
@@ -553,8 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 static_assert(2 * 128 / 32 * 16384 <= 4 * 32768, "dK/dV staging must stay below the dO stages");
 
 template <int D, int GM>
-void launch_prep(const BwdParams& P, long long blocks, cudaStream_t s) {
-  attn_bwd_prep_kernel<D, GM><<<(unsigned)blocks, 256, 0, s>>>(P);
+void launch_prep(const BwdParams& P, cudaStream_t s) {
+  const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
+  using S = PrepShape<GM>;
+  const long long per_block = (S::kThreads / 32) * (32 / (D / S::E));
+  long long blocks = (rows + per_block - 1) / per_block;
+  if (blocks > 152 * 64) blocks = 152 * 64;  // grid-stride beyond that
+  attn_bwd_prep_kernel<D, GM><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
 }
 
 template <int D>
@@ -598,18 +672,15 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   if ((e = encode_f32_map(&tmDV, g.dv_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
 
-  const long long rows = (long long)a.B * a.H_kv * a.Q_LEN;
-  long long blocks = (rows + 7) / 8;
-  if (blocks > 152 * 32) blocks = 152 * 32;
   prof_before(s, STT_KERNEL_ATTN_BWD_PREP);
   if (P.G == 1)
-    launch_prep<D, 1>(P, blocks, s);
+    launch_prep<D, 1>(P, s);
   else if (P.G == 2)
-    launch_prep<D, 2>(P, blocks, s);
+    launch_prep<D, 2>(P, s);
   else if (P.G <= 4)
-    launch_prep<D, 4>(P, blocks, s);
+    launch_prep<D, 4>(P, s);
   else
-    launch_prep<D, 8>(P, blocks, s);
+    launch_prep<D, 8>(P, s);
   prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
