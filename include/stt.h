@@ -206,10 +206,13 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_KERNEL_ATTN_BWD_PREP 4
 #define STT_KERNEL_ATTN_BWD_CAUSAL 5
 
-/* Device error-word bits (sites of bounded waits). */
+/* Device error-word bits: sites of bounded waits that gave up, and blocks
+ * whose dynamic shared memory did not have the 1024-byte alignment the
+ * swizzled tiles need (such a block skips its work). */
 #define STT_DEVERR_FWD_WAIT 0x1u
 #define STT_DEVERR_BWD_WAIT 0x2u
 #define STT_DEVERR_CE_WAIT 0x4u
+#define STT_DEVERR_SMEM_ALIGN 0x8u
 
 #ifdef __cplusplus
 }

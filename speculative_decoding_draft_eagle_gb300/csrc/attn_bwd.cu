@@ -15,14 +15,17 @@
 //      dK_0 / dV_0 zeroed for the causal kernel's accumulation.
 //   2. causal (tcgen05, one CTA per 128-row key tile of a query head, looping
 //      over the query tiles that see it): S^T = K Q^T and dP^T = V dO^T in
-//      TMEM; 8 compute warps form P^T (written back into TMEM as bf16) and
-//      dS^T (written to shared memory as bf16); then dV += P^T dO (A from
-//      TMEM), dK += dS^T Q and dQ = dS K (A = the same dS^T tile read
-//      MN-major, i.e. transposed) run on the tensor cores.  dV and dK stay in
-//      TMEM across the query tiles.  Each tile's dQ is staged in shared memory
-//      and added to the fp32 dq by TMA reduce-add; the final dK / dV of the
-//      key tile are reduce-added the same way into dK_0 / dV_0, summing the
-//      group's query heads.
+//      TMEM; 8 compute warps form P^T (written back into TMEM as bf16), then
+//      dS^T (written to shared memory as bf16); dV += P^T dO (A from TMEM),
+//      dK += dS^T Q and dQ = dS K (A = the dS^T tile read MN-major, i.e.
+//      transposed) run on the tensor cores.  The MMA warp issues S^T(i+1)
+//      right after dV(i), so it runs while the compute warps form dS(i).  dV
+//      and dK stay in TMEM across the query tiles.  Each tile's dQ is read out
+//      of TMEM, staged in shared memory and added to the fp32 dq by TMA
+//      reduce-add (issued by the producer warp, which releases each staging
+//      buffer as soon as TMA has read it); the final dK / dV of the key tile
+//      are reduce-added the same way into dK_0 / dV_0, summing the group's
+//      query heads.
 // Every causal score entry costs 5 tensor-core products (the useful 10*D
 // flops); dq, dK_0 and dV_0 receive their partial sums in arrival order.
 #include "../../include/stt.h"
@@ -253,26 +256,46 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
 }
 
 // ---------------------------------------------------------------- causal --
-// TMEM columns: S^T (P^T is written back into it), dP^T (reused for this
+// TMEM columns: S^T (P^T is written back into it), dP^T (reused for the
 // tile's dQ), dV, dK.  Column half h of P^T lives in S^T columns
 // [64h, 64h + 32), inside the S^T columns its own warps read, so the write-back
 // needs no barrier between the two halves.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
+// Shared memory: K and V of the key tile, two stages of Q and dO, the dS^T
+// tile.  A query tile's dQ leaves through fp32 staging blocks of [128 x 32]
+// (16 KB; block h holds 32 columns of compute half h): part A in the dS^T
+// buffer (free once dK and dQ of the tile are done; TMA reads it first, so it
+// is free again before the next dS^T), and for D = 128 part B in the tile's dO
+// buffer (free once dV is done; reloaded only after TMA has read it).
 template <int D>
 struct CausalSmem {
   static constexpr int kTileB = kTile * D * 2;  // one 128 x D bf16 tile
   static constexpr int kDsB = kTile * kTile * 2;
   static constexpr int kStages = 2;
+  static constexpr int kParts = D / 64;
+  static constexpr int kStageBlkB = kTile * 32 * 4;
   static constexpr int k = 0;
   static constexpr int v = kTileB;
   static constexpr int q0 = 2 * kTileB;
-  static constexpr int do0 = 2 * kTileB + kStages * kTileB;
-  static constexpr int ds = 2 * kTileB + 2 * kStages * kTileB;
+  static constexpr int do0 = q0 + kStages * kTileB;
+  static constexpr int ds = do0 + kStages * kTileB;
   static constexpr int total = ds + kDsB;
-  static constexpr int alloc = total + 1024;
+  static constexpr int alloc = total;  // the dynamic array is declared 1024-byte aligned
+  static_assert(2 * kStageBlkB == kDsB, "staging part A fills the dS^T buffer");
+  static_assert(D == 64 || 2 * kStageBlkB == kTileB, "staging part B fills one dO buffer");
+  // The final dK / dV staging (2 x D/32 blocks) overwrites K, V and the Q
+  // stages only, never a buffer the last dQ reduction may still read.
+  static_assert(2 * (D / 32) * kStageBlkB <= do0, "dK/dV staging must stay below the dO stages");
 };
+
+// Staging part p (0: dS^T buffer, 1: dO buffer of stage st).
+template <int D>
+__device__ __forceinline__ unsigned char* dq_staging(unsigned char* smem, int p, int st) {
+  using L = CausalSmem<D>;
+  return p == 0 ? smem + L::ds : smem + L::do0 + st * L::kTileB;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -286,13 +309,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tmDV) {
   using L = CausalSmem<D>;
   constexpr int NS = L::kStages;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv, bar_qdo_full[NS], bar_qdo_empty[NS], bar_sdp_full, bar_pds_ready,
-      bar_acc_done, bar_dq_free, bar_stage_free, bar_drain, bar_grp;
+  constexpr int NP = L::kParts;
+  // The swizzled tiles need 1024-byte alignment, which the declaration asks
+  // of the launch; a block that does not get it does no work and reports it.
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw;
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(STT_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  // Producer -> MMA: kv, q_full, do_full.  MMA -> producer: q_empty.
+  // MMA -> compute: s_full, dp_full, dq_full, dk_done, final.  Compute -> MMA:
+  // p_ready, ds_ready, dq_free.  Compute -> producer: stg_full; producer ->
+  // compute: stg_free (staging part A read).  MMA -> itself: pt_free, drain.
+  // Compute group: grp.
+  __shared__ uint64_t bar_kv, bar_q_full[NS], bar_do_full[NS], bar_q_empty[NS], bar_s_full,
+      bar_dp_full, bar_p_ready, bar_pt_free, bar_ds_ready, bar_dq_full, bar_dk_done, bar_dq_free,
+      bar_stg_full, bar_stg_free, bar_final, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
-  __shared__ __align__(16) float s_stat[2][kTile];  // [lse2 | Delta][query] of the current tile
+  // [tile parity][lse2 | Delta][query]: tile i's statistics sit in buffer i & 1.
+  __shared__ __align__(16) float s_stat[2][2][kTile];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -307,14 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&bar_qdo_full[s], 1);
-      mbar_init(&bar_qdo_empty[s], 1);
+      mbar_init(&bar_q_full[s], 1);
+      mbar_init(&bar_do_full[s], 1);
+      mbar_init(&bar_q_empty[s], 1);
     }
-    mbar_init(&bar_sdp_full, 1);
-    mbar_init(&bar_pds_ready, kComputeWarps);
-    mbar_init(&bar_acc_done, 1);
+    mbar_init(&bar_s_full, 1);
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_p_ready, kComputeWarps);
+    mbar_init(&bar_pt_free, 1);
+    mbar_init(&bar_ds_ready, kComputeWarps);
+    mbar_init(&bar_dq_full, 1);
+    mbar_init(&bar_dk_done, 1);
     mbar_init(&bar_dq_free, kComputeWarps);
-    mbar_init(&bar_stage_free, 1);
+    mbar_init(&bar_stg_full, kComputeWarps);
+    mbar_init(&bar_stg_free, 1);
+    mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_grp, kComputeWarps);
     fence_mbar_init();
@@ -329,58 +372,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base;
 
   if (warp == kWarpTma) {
-    // ------------------------------------------------------ TMA producer --
+    // ------------------------------------------- TMA producer and dQ adds --
     if (lane == 0 && n_q > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDQ);
       const int bhk = b * P.H_kv + hk;
       mbar_arrive_expect_tx(&bar_kv, 2 * L::kTileB);
       for (int cb = 0; cb < D / kColBlock; ++cb) {
         tma_load_3d(smem + L::k + cb * kTile * 128, &tmK, &bar_kv, cb * kColBlock, c0, bhk);
         tma_load_3d(smem + L::v + cb * kTile * 128, &tmV, &bar_kv, cb * kColBlock, c0, bhk);
       }
-      int issued = 0;
-      for (int i = 0; i < n_q; ++i) {
+      auto load_q = [&](int i) {
         const int st = i % NS;
-        const int tq = (t_first + i) * kTile;
-        // The stage is released once its tile's MMAs are done and the dQ
-        // staging that borrows the dO buffer has been read by TMA.
-        if (i >= NS &&
-            !mbar_wait(&bar_qdo_empty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, STT_DEVERR_BWD_WAIT))
-          break;
-        mbar_arrive_expect_tx(&bar_qdo_full[st], 2 * L::kTileB);
-        for (int cb = 0; cb < D / kColBlock; ++cb) {
-          tma_load_3d(smem + L::q0 + st * L::kTileB + cb * kTile * 128, &tmQ, &bar_qdo_full[st],
-                      cb * kColBlock, tq, bh);
-          tma_load_3d(smem + L::do0 + st * L::kTileB + cb * kTile * 128, &tmDO, &bar_qdo_full[st],
-                      cb * kColBlock, tq, bh);
-        }
-        ++issued;
+        mbar_arrive_expect_tx(&bar_q_full[st], L::kTileB);
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_load_3d(smem + L::q0 + st * L::kTileB + cb * kTile * 128, &tmQ, &bar_q_full[st],
+                      cb * kColBlock, (t_first + i) * kTile, bh);
+      };
+      auto load_do = [&](int i) {
+        const int st = i % NS;
+        mbar_arrive_expect_tx(&bar_do_full[st], L::kTileB);
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_load_3d(smem + L::do0 + st * L::kTileB + cb * kTile * 128, &tmDO, &bar_do_full[st],
+                      cb * kColBlock, (t_first + i) * kTile, bh);
+      };
+      int issued_q = 0, issued_do = 0;
+      for (; issued_q < NS && issued_q < n_q; ++issued_q) {
+        load_q(issued_q);
+        load_do(issued_q);
+        ++issued_do;
       }
-      if (issued < n_q) {
+      bool ok = true;
+      for (int i = 0; ok && i < n_q; ++i) {
+        const int st = i % NS;
+        const int tq0 = (t_first + i) * kTile;
+        // dQ of tile i: part p, block hh holds columns [hh D/2 + 32 p, +32).
+        ok = mbar_wait(&bar_stg_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+        if (!ok) break;
+        for (int p = 0; p < NP; ++p) {
+          unsigned char* sb = dq_staging<D>(smem, p, st);
+          for (int hh = 0; hh < 2; ++hh)
+            tma_reduce_add_3d(&tmDQ, sb + hh * L::kStageBlkB, hh * (D / 2) + 32 * p, tq0, bh);
+          bulk_commit_group();
+        }
+        // Q(i) is free once dK(i) is done (before the staging of part A).
+        const bool more = i + NS < n_q;
+        if (more) {
+          ok = mbar_wait(&bar_q_empty[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+          load_q(i + NS);
+          ++issued_q;
+        }
+        // Part A read: the compute warps may write the next dS^T.
+        if constexpr (NP == 2)
+          bulk_wait_group_read1();
+        else
+          bulk_wait_group_read0();
+        mbar_arrive(&bar_stg_free);
+        if (more) {
+          // Part B read: dO(i)'s buffer takes dO(i + NS).
+          bulk_wait_group_read0();
+          load_do(i + NS);
+          ++issued_do;
+        }
+      }
+      if (!ok) {
         // Gave up: let every copy already issued land before the CTA exits.
         mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
-        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
-          mbar_wait(&bar_qdo_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
+        for (int i = (issued_q > NS ? issued_q - NS : 0); i < issued_q; ++i)
+          mbar_wait(&bar_q_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
+        for (int i = (issued_do > NS ? issued_do - NS : 0); i < issued_do; ++i)
+          mbar_wait(&bar_do_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
       }
+      bulk_wait_group0();
     }
   } else if (warp == kWarpMma) {
     // -------------------------------------------------------- MMA issuer --
+    // Per query tile i: dP^T(i) once dQ(i-1) is out of TMEM, dV(i) once P^T(i)
+    // is in TMEM, S^T(i+1) as soon as dV(i) has consumed P^T(i) (it runs while
+    // the compute warps form dS(i)), then dQ(i) and dK(i) once dS^T(i) is in
+    // shared memory (dQ first: its read-out overlaps dK).
     if (lane == 0 && n_q > 0) {
       const uint32_t idSS = idesc_bf16(128, kTile, false, false);  // S^T, dP^T
       const uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK (B MN-major)
       const uint32_t idQ = idesc_bf16(128, D, true, true);         // dQ (A, B MN-major)
       const uint32_t aK = smem_u32(smem + L::k), aV = smem_u32(smem + L::v);
       const uint32_t aDS = smem_u32(smem + L::ds);
-      bool ok = mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
+      // S^T(t) = K Q(t)^T into the S^T columns.
+      auto issue_s = [&](int t) -> bool {
+        const int s = t % NS;
+        if (!mbar_wait(&bar_q_full[s], (uint32_t)(t / NS) & 1u, STT_DEVERR_BWD_WAIT)) return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(smem + L::q0 + s * L::kTileB);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
+          umma_bf16_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024),
+                       sdesc_sw128(aQ + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar_s_full);
+        return true;
+      };
+      bool ok = mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT) && issue_s(0);
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % NS;
-        const uint32_t par = (uint32_t)(i - 1) & 1u;
-        ok = mbar_wait(&bar_qdo_full[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
-        // P^T and dS^T of the previous tile consumed by its MMAs.
-        if (ok && i > 0) ok = mbar_wait(&bar_acc_done, par, STT_DEVERR_BWD_WAIT);
+        const uint32_t par = (uint32_t)i & 1u;
+        ok = mbar_wait(&bar_do_full[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
+        // dQ(i-1) has been read out of the dP^T columns.
+        if (ok && i > 0) ok = mbar_wait(&bar_dq_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         tc_fence_after();
         const uint32_t aQ = smem_u32(smem + L::q0 + st * L::kTileB);
@@ -388,23 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024),
-                       sdesc_sw128(aQ + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
-        }
-        // The previous tile's dQ has been read out of the dP^T columns.
-        if (i > 0 && !mbar_wait(&bar_dq_free, par, STT_DEVERR_BWD_WAIT)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
           umma_bf16_ss(tmem + kColDP, sdesc_sw128(aV + off, 16, 1024),
                        sdesc_sw128(aDO + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bar_sdp_full);
-        ok = mbar_wait(&bar_pds_ready, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+        umma_commit(&bar_dp_full);
+        ok = mbar_wait(&bar_p_ready, par, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         tc_fence_after();
         // dV += P^T dO: A = P^T in TMEM (8 columns per 16 queries; queries
@@ -414,6 +504,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                        sdesc_sw128(aDO + kk * 2048, kTile * 128, 1024), idKV,
                        (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar_pt_free);
+        if (i + 1 < n_q) {
+          // P^T(i) consumed: S^T(i+1) may overwrite the S^T columns.
+          ok = mbar_wait(&bar_pt_free, par, STT_DEVERR_BWD_WAIT) && issue_s(i + 1);
+          if (!ok) break;
+        }
+        ok = mbar_wait(&bar_ds_ready, par, STT_DEVERR_BWD_WAIT);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ = dS K: A = the dS^T tile read MN-major (rows = keys = K dim),
+        // B = K MN-major; into the dP^T columns.
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aDS + kk * 2048, kTile * 128, 1024),
+                       sdesc_sw128(aK + kk * 2048, kTile * 128, 1024), idQ, kk > 0 ? 1u : 0u);
+        umma_commit(&bar_dq_full);
         // dK += dS^T Q: A = dS^T in smem (K-major over queries), B = Q MN-major.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
@@ -421,14 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sdesc_sw128(aDS + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024),
                        sdesc_sw128(aQ + kk * 2048, kTile * 128, 1024), idKV,
                        (i > 0 || kk > 0) ? 1u : 0u);
-        // dQ = dS K: A = the same dS^T tile read MN-major (rows = keys = K dim),
-        // B = K MN-major; into the dP^T columns.
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aDS + kk * 2048, kTile * 128, 1024),
-                       sdesc_sw128(aK + kk * 2048, kTile * 128, 1024), idQ, kk > 0 ? 1u : 0u);
-        umma_commit(&bar_acc_done);
+        umma_commit(&bar_q_empty[st]);
+        umma_commit(&bar_dk_done);
       }
+      if (ok) umma_commit(&bar_final);
       // Every MMA issued by this thread is complete before TMEM is released.
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
@@ -445,171 +547,195 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool kv_live = kv < T;  // T <= Q_LEN, so also kv < Q_LEN
     unsigned char* sDS = smem + L::ds;
     // Thread tid stages one statistic of one query of a tile: lse2 (tid < 128)
-    // or Delta (tid >= 128) of query tq0 + (tid & 127).
+    // or Delta (tid >= 128) of query tq0 + (tid & 127).  The raw value is
+    // fetched a tile ahead and scaled only when it is stored.
     const int st_which = tid >> 7, st_idx = tid & 127;
     auto fetch_stat = [&](int i) -> float {
       const int qq = (t_first + i) * kTile + st_idx;
       if (qq >= P.Q_LEN) return 0.f;
       const size_t rq = (size_t)bh * P.Q_LEN + qq;
-      return st_which == 0 ? P.lse[rq] * kLog2e : P.delta[rq];
+      return st_which == 0 ? P.lse[rq] : P.delta[rq];
+    };
+    auto put_stat = [&](int buf, float raw) {
+      s_stat[buf][st_which][st_idx] = st_which == 0 ? raw * kLog2e : raw;
     };
     uint32_t grp_uses = 0;
     bool ok = true;
     float stat_next = 0.f;
     if (n_q > 0) {
-      s_stat[st_which][st_idx] = fetch_stat(0);
-      if (n_q > 1) stat_next = fetch_stat(1);
+      put_stat(0, fetch_stat(0));
+      if (n_q > 1) put_stat(1, fetch_stat(1));
+      if (n_q > 2) stat_next = fetch_stat(2);
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
     }
     for (int i = 0; ok && i < n_q; ++i) {
       const int st = i % NS;
+      const uint32_t par = (uint32_t)i & 1u;
       const int tq0 = (t_first + i) * kTile;
       const int qh = tq0 + half * 64;  // first query of this thread's half
-      // Every compute thread finished the previous tile: this tile's
-      // statistics are in shared memory.
-      if (i > 0) {
-        ok = warp_wait(&bar_dq_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-      }
-      ok = warp_wait(&bar_sdp_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
-      tc_fence_after();
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
       const bool full = kv_live && kv <= qh && qh + 64 <= P.Q_LEN;
-      const float* lse_s = s_stat[0] + half * 64;
-      const float* dl_s = s_stat[1] + half * 64;
-      uint32_t dd[2][16];  // dS^T of both chunks, stored once the staging buffer is free
+      const float* lse_s = s_stat[par][0] + half * 64;
+      const float* dl_s = s_stat[par][1] + half * 64;
+
+      // ---- P^T = exp(S^T - lse): queries [qh, qh + 64) of key row kv
+      ok = warp_wait(&bar_s_full, par, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      tc_fence_after();
+      float pf[64];
+      {
+        uint32_t s[2][32];
+        tmem_ld32x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColS + half * 64 + 32,
+                    s[0], s[1]);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t pp[16];
+#pragma unroll
+          for (int x4 = 0; x4 < 32; x4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pv = ex2(fmaf(__uint_as_float(s[c2][x4 + e]), sl2, -lv[e]));
+              if (!full) {
+                const int qa = qh + c2 * 32 + x4 + e;
+                if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv = 0.f;
+              }
+              pf[c2 * 32 + x4 + e] = pv;
+            }
+            pp[x4 >> 1] = pack_bf16(pf[c2 * 32 + x4], pf[c2 * 32 + x4 + 1]);
+            pp[(x4 >> 1) + 1] = pack_bf16(pf[c2 * 32 + x4 + 2], pf[c2 * 32 + x4 + 3]);
+          }
+          // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
+          tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&bar_p_ready);
+
+      // ---- dS^T = P^T (dP^T - Delta) -> swizzled [key][query] tile in smem.
+      ok = warp_wait(&bar_dp_full, par, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dd[2][16];
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t s[32], dp[32], pp[16];
-        tmem_ld32x2(tmem + lane_off + kColS + half * 64 + c2 * 32,
-                    tmem + lane_off + kColDP + half * 64 + c2 * 32, s, dp);
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_off + kColDP + half * 64 + c2 * 32, dp);
 #pragma unroll
         for (int x4 = 0; x4 < 32; x4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
           const float4 d4 = *reinterpret_cast<const float4*>(dl_s + c2 * 32 + x4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], sv[4];
+          float sv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pv[e] = ex2(fmaf(__uint_as_float(s[x4 + e]), sl2, -lv[e]));
-            if (!full) {
-              const int qa = qh + c2 * 32 + x4 + e;
-              if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv[e] = 0.f;
-            }
-            sv[e] = pv[e] * (__uint_as_float(dp[x4 + e]) - dv[e]);
-          }
-          pp[x4 >> 1] = pack_bf16(pv[0], pv[1]);
-          pp[(x4 >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+          for (int e = 0; e < 4; ++e)
+            sv[e] = pf[c2 * 32 + x4 + e] * (__uint_as_float(dp[x4 + e]) - dv[e]);
           dd[c2][x4 >> 1] = pack_bf16(sv[0], sv[1]);
           dd[c2][(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
         }
-        // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
-        tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
       }
+      // The dS^T buffer held the previous tile's dQ staging (part A) until
+      // TMA read it.
       if (i > 0) {
-        // The dS^T buffer (and the previous tile's dO buffer) hold the
-        // previous tile's dQ staging until TMA has read them.
-        if (tid == 0) {
-          bulk_wait_group_read0();
-          mbar_arrive(&bar_stage_free);
-          mbar_arrive(&bar_qdo_empty[(i - 1) % NS]);
-        }
-        ok = warp_wait(&bar_stage_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+        ok = warp_wait(&bar_stg_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
       }
-      // dS^T row kv, queries [qh, qh + 64) -> swizzled [key][query] tile
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           *reinterpret_cast<uint4*>(sDS + swz_chunk_offset(r, half * 8 + c2 * 4 + w, kTile)) =
               make_uint4(dd[c2][4 * w], dd[c2][4 * w + 1], dd[c2][4 * w + 2], dd[c2][4 * w + 3]);
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      warp_arrive(&bar_pds_ready);
+      warp_arrive(&bar_ds_ready);
 
-      // Statistics of the next tile, once every warp is done with this one's.
-      ok = warp_wait(&bar_pds_ready, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+      // Every warp is done with this tile's statistics: its buffer takes
+      // those of tile i + 2, which the next tile's ds_ready barrier publishes.
+      ok = warp_wait(&bar_ds_ready, par, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
-      if (i + 1 < n_q) {
-        s_stat[st_which][st_idx] = stat_next;
-        if (i + 2 < n_q) stat_next = fetch_stat(i + 2);
+      if (i + 2 < n_q) {
+        put_stat(par, stat_next);
+        if (i + 3 < n_q) stat_next = fetch_stat(i + 3);
       }
 
-      // This tile's dQ (rows = queries tq0 + r), staged as swizzled [128 x 32]
-      // fp32 blocks: the 64 columns of half h go to the dS^T buffer (pass 0) and
-      // the dO buffer of this tile (pass 1), both free once the MMAs are done.
-      ok = warp_wait(&bar_acc_done, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+      // ---- dQ of this tile (rows = queries tq0 + r): read out of TMEM, then
+      // staged as [128 x 32] fp32 blocks for the producer's TMA reduce-add.
+      ok = warp_wait(&bar_dq_full, par, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      unsigned char* stage[2] = {sDS, smem + L::do0 + st * L::kTileB};
-#pragma unroll
-      for (int pss = 0; pss < D / 64; ++pss) {
-        const int cc = half * (D / 64) + pss;  // this thread's 32-column chunk
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + kColDP + cc * 32, u);
-        unsigned char* blk = stage[pss] + half * (kTile * 128);
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
-              P.scale * __uint_as_float(u[4 * w]), P.scale * __uint_as_float(u[4 * w + 1]),
-              P.scale * __uint_as_float(u[4 * w + 2]), P.scale * __uint_as_float(u[4 * w + 3]));
-      }
+      uint32_t u[NP][32];
+      if constexpr (NP == 2)
+        tmem_ld32x2(tmem + lane_off + kColDP + half * 64, tmem + lane_off + kColDP + half * 64 + 32,
+                    u[0], u[NP - 1]);
+      else
+        tmem_ld32(tmem + lane_off + kColDP + half * 32, u[0]);
       // dQ is out of TMEM: the MMA warp may overwrite the dP^T columns.
       tc_fence_before();
       warp_arrive(&bar_dq_free);
-      fence_proxy_async_smem();
-      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
-      if (tid == 0) {
+      // Part B (the dO buffer, free since dV) first; part A (the dS^T buffer)
+      // once dK, its last reader, is done.
 #pragma unroll
-        for (int pss = 0; pss < D / 64; ++pss) {
-          tma_reduce_add_3d(&tmDQ, stage[pss], pss * 32, tq0, bh);
-          tma_reduce_add_3d(&tmDQ, stage[pss] + kTile * 128, (D / 64 + pss) * 32, tq0, bh);
+      for (int p = NP - 1; p >= 0; --p) {
+        if (p == 0) {
+          ok = warp_wait(&bar_dk_done, par, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
         }
-        bulk_commit_group();
+        unsigned char* blk = dq_staging<D>(smem, p, st) + half * L::kStageBlkB;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+          *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
+              P.scale * __uint_as_float(u[p][4 * w]), P.scale * __uint_as_float(u[p][4 * w + 1]),
+              P.scale * __uint_as_float(u[p][4 * w + 2]), P.scale * __uint_as_float(u[p][4 * w + 3]));
       }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      warp_arrive(&bar_stg_full);
     }
     if (ok && n_q > 0) {
       // dV and dK of this key tile into the block-0 gradients, summed over the
-      // group's query heads: K, V and the Q stages are free now, so all D/32
-      // chunks of both are staged at once (below the dO stages, which may
-      // still be read by the last dQ reduction) and reduce-added by TMA (rows
-      // kv >= T hold zeros; rows past Q_LEN are clipped).
+      // group's query heads: every MMA is done, so K, V and the Q stages are
+      // free and all D/32 chunks of both are staged at once (below the dO
+      // stages and the dS^T buffer, which the last dQ reduction may still
+      // read) and reduce-added by TMA (rows kv >= T hold zeros; rows past
+      // Q_LEN are clipped).
+      ok = warp_wait(&bar_final, 0, STT_DEVERR_BWD_WAIT);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        const int cc = half * (D / 64) + c2;
-        uint32_t uv[32], uk[32];
-        tmem_ld32x2(tmem + lane_off + kColDV + cc * 32, tmem + lane_off + kColDK + cc * 32, uv, uk);
-        unsigned char* bv = smem + cc * (kTile * 128);
-        unsigned char* bk = smem + (D / 32 + cc) * (kTile * 128);
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          const int cc = half * (D / 64) + c2;
+          uint32_t uv[32], uk[32];
+          tmem_ld32x2(tmem + lane_off + kColDV + cc * 32, tmem + lane_off + kColDK + cc * 32, uv, uk);
+          unsigned char* bv = smem + cc * L::kStageBlkB;
+          unsigned char* bk = smem + (D / 32 + cc) * L::kStageBlkB;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const uint32_t o = swz128(r, w);
-          *reinterpret_cast<float4*>(bv + o) =
-              make_float4(__uint_as_float(uv[4 * w]), __uint_as_float(uv[4 * w + 1]),
-                          __uint_as_float(uv[4 * w + 2]), __uint_as_float(uv[4 * w + 3]));
-          *reinterpret_cast<float4*>(bk + o) = make_float4(
-              P.scale * __uint_as_float(uk[4 * w]), P.scale * __uint_as_float(uk[4 * w + 1]),
-              P.scale * __uint_as_float(uk[4 * w + 2]), P.scale * __uint_as_float(uk[4 * w + 3]));
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t o = swz128(r, w);
+            *reinterpret_cast<float4*>(bv + o) =
+                make_float4(__uint_as_float(uv[4 * w]), __uint_as_float(uv[4 * w + 1]),
+                            __uint_as_float(uv[4 * w + 2]), __uint_as_float(uv[4 * w + 3]));
+            *reinterpret_cast<float4*>(bk + o) = make_float4(
+                P.scale * __uint_as_float(uk[4 * w]), P.scale * __uint_as_float(uk[4 * w + 1]),
+                P.scale * __uint_as_float(uk[4 * w + 2]), P.scale * __uint_as_float(uk[4 * w + 3]));
+          }
         }
+        fence_proxy_async_smem();
+        ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
       }
-      fence_proxy_async_smem();
-      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
       if (ok && tid == 0) {
         const int bhk = b * P.H_kv + hk;
         for (int cc = 0; cc < D / 32; ++cc) {
-          tma_reduce_add_3d(&tmDV, smem + cc * (kTile * 128), cc * 32, c0, bhk);
-          tma_reduce_add_3d(&tmDK, smem + (D / 32 + cc) * (kTile * 128), cc * 32, c0, bhk);
+          tma_reduce_add_3d(&tmDV, smem + cc * L::kStageBlkB, cc * 32, c0, bhk);
+          tma_reduce_add_3d(&tmDK, smem + (D / 32 + cc) * L::kStageBlkB, cc * 32, c0, bhk);
         }
         bulk_commit_group();
+        // The issuing thread waits for its reductions before the CTA's shared
+        // memory goes away.
+        bulk_wait_group0();
       }
     }
-    // The issuing thread waits for its reductions before the CTA's shared memory goes away.
-    if (tid == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -618,8 +744,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
-
-static_assert(2 * 128 / 32 * 16384 <= 4 * 32768, "dK/dV staging must stay below the dO stages");
 
 template <int D, int GM>
 void launch_prep(const BwdParams& P, cudaStream_t s) {
