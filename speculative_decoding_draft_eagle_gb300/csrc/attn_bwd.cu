@@ -34,10 +34,11 @@
 namespace stt {
 namespace {
 
-constexpr int kThreads = 320;   // warps 0-7 compute, 8 TMA, 9 MMA
+constexpr int kThreads = 448;   // warps 0-7 compute, 8 TMA, 9 MMA, 10-13 dQ epilogue
 constexpr int kCompute = 256;
 constexpr int kComputeWarps = kCompute / 32;  // barriers count one arrival per warp
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
+constexpr int kEpiWarps = 4;  // one per TMEM lane quarter (warp % 4)
 
 struct BwdParams {
   const __nv_bfloat16* q;
@@ -319,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   // Producer -> MMA: kv, q_full, do_full.  MMA -> producer: q_empty.
-  // MMA -> compute: s_full, dp_full, dq_full, dk_done, final.  Compute -> MMA:
-  // p_ready, ds_ready, dq_free.  Compute -> producer: stg_full; producer ->
-  // compute: stg_free (staging part A read).  MMA -> itself: pt_free, drain.
-  // Compute group: grp.
+  // MMA -> compute: s_full, dp_full, final.  Compute -> MMA: p_ready,
+  // ds_ready.  MMA -> epilogue: dq_full, dk_done.  Epilogue -> MMA: dq_free.
+  // Epilogue -> producer: stg_full; producer -> compute: stg_free (staging
+  // part A read).  MMA -> itself: pt_free, drain.  Compute group: grp.
   __shared__ uint64_t bar_kv, bar_q_full[NS], bar_do_full[NS], bar_q_empty[NS], bar_s_full,
       bar_dp_full, bar_p_ready, bar_pt_free, bar_ds_ready, bar_dq_full, bar_dk_done, bar_dq_free,
       bar_stg_full, bar_stg_free, bar_final, bar_drain, bar_grp;
@@ -354,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_ds_ready, kComputeWarps);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dk_done, 1);
-    mbar_init(&bar_dq_free, kComputeWarps);
-    mbar_init(&bar_stg_full, kComputeWarps);
+    mbar_init(&bar_dq_free, kEpiWarps);
+    mbar_init(&bar_stg_full, kEpiWarps);
     mbar_init(&bar_stg_free, 1);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_drain, 1);
@@ -409,6 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % NS;
         const int tq0 = (t_first + i) * kTile;
+        // Q(i) is free once dK(i) is done, before the staging of part A; its
+        // successor is loaded first, ahead of the reductions in TMA's queue.
+        const bool more = i + NS < n_q;
+        if (more) {
+          ok = mbar_wait(&bar_q_empty[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+          load_q(i + NS);
+          ++issued_q;
+        }
         // dQ of tile i: part p, block hh holds columns [hh D/2 + 32 p, +32).
         ok = mbar_wait(&bar_stg_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
@@ -417,14 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hh = 0; hh < 2; ++hh)
             tma_reduce_add_3d(&tmDQ, sb + hh * L::kStageBlkB, hh * (D / 2) + 32 * p, tq0, bh);
           bulk_commit_group();
-        }
-        // Q(i) is free once dK(i) is done (before the staging of part A).
-        const bool more = i + NS < n_q;
-        if (more) {
-          ok = mbar_wait(&bar_q_empty[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
-          if (!ok) break;
-          load_q(i + NS);
-          ++issued_q;
         }
         // Part A read: the compute warps may write the next dS^T.
         if constexpr (NP == 2)
@@ -535,10 +537,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
     }
+  } else if (warp >= kWarpEpi) {
+    // ------------------------------------------------------- dQ epilogue --
+    // Thread = query row r of TMEM lane quarter warp % 4.  Per tile: the
+    // columns of staging part B (the dO buffer, free since dV) go first, then
+    // the part A columns are read into registers, TMEM is released to dP^T of
+    // the next tile, and part A (the dS^T buffer) is written once dK, its last
+    // reader, is done.  Staging part p, block hh holds dQ columns
+    // [hh D/2 + 32 p, +32) of all 128 rows.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto stage = [&](unsigned char* blk, const uint32_t (&u)[32]) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
+            P.scale * __uint_as_float(u[4 * w]), P.scale * __uint_as_float(u[4 * w + 1]),
+            P.scale * __uint_as_float(u[4 * w + 2]), P.scale * __uint_as_float(u[4 * w + 3]));
+    };
+    bool ok = true;
+    for (int i = 0; ok && i < n_q; ++i) {
+      const int st = i % NS;
+      const uint32_t par = (uint32_t)i & 1u;
+      ok = warp_wait(&bar_dq_full, par, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (NP == 2) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_off + kColDP + hh * (D / 2) + 32, u);
+          stage(dq_staging<D>(smem, 1, st) + hh * L::kStageBlkB, u);
+        }
+      }
+      uint32_t a0[32], a1[32];
+      tmem_ld32x2(tmem + lane_off + kColDP, tmem + lane_off + kColDP + D / 2, a0, a1);
+      // dQ is out of TMEM: the MMA warp may overwrite the dP^T columns.
+      tc_fence_before();
+      warp_arrive(&bar_dq_free);
+      ok = warp_wait(&bar_dk_done, par, STT_DEVERR_BWD_WAIT);
+      if (!ok) break;
+      stage(dq_staging<D>(smem, 0, st), a0);
+      stage(dq_staging<D>(smem, 0, st) + L::kStageBlkB, a1);
+      fence_proxy_async_smem();
+      warp_arrive(&bar_stg_full);
+    }
   } else {
     // ------------------------------------------------------ compute warps --
-    // Row r of the TMEM lane quarter is key row c0 + r for S^T / dP^T / dV / dK
-    // and query row tq0 + r for dQ; `half` selects the 64-column half.
+    // Row r of the TMEM lane quarter is key row c0 + r for S^T / dP^T / dV /
+    // dK; `half` selects the 64-query half of the tile.
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;
     const int kv = c0 + r;
@@ -569,7 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_BWD_WAIT);
     }
     for (int i = 0; ok && i < n_q; ++i) {
-      const int st = i % NS;
       const uint32_t par = (uint32_t)i & 1u;
       const int tq0 = (t_first + i) * kTile;
       const int qh = tq0 + half * 64;  // first query of this thread's half
@@ -578,50 +624,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* lse_s = s_stat[par][0] + half * 64;
       const float* dl_s = s_stat[par][1] + half * 64;
 
-      // ---- P^T = exp(S^T - lse): queries [qh, qh + 64) of key row kv
+      // ---- P^T = exp(S^T - lse): queries [qh, qh + 64) of key row kv.  The
+      // fp32 P overwrites the loaded S^T values (it is needed again for dS).
       ok = warp_wait(&bar_s_full, par, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      float pf[64];
-      {
-        uint32_t s[2][32];
-        tmem_ld32x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColS + half * 64 + 32,
-                    s[0], s[1]);
+      uint32_t pf[2][32];
+      tmem_ld32x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColS + half * 64 + 32,
+                  pf[0], pf[1]);
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t pp[16];
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t pp[16];
 #pragma unroll
-          for (int x4 = 0; x4 < 32; x4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int x4 = 0; x4 < 32; x4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pv = ex2(fmaf(__uint_as_float(s[c2][x4 + e]), sl2, -lv[e]));
-              if (!full) {
-                const int qa = qh + c2 * 32 + x4 + e;
-                if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv = 0.f;
-              }
-              pf[c2 * 32 + x4 + e] = pv;
+          for (int e = 0; e < 4; ++e) {
+            float pv = ex2(fmaf(__uint_as_float(pf[c2][x4 + e]), sl2, -lv[e]));
+            if (!full) {
+              const int qa = qh + c2 * 32 + x4 + e;
+              if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv = 0.f;
             }
-            pp[x4 >> 1] = pack_bf16(pf[c2 * 32 + x4], pf[c2 * 32 + x4 + 1]);
-            pp[(x4 >> 1) + 1] = pack_bf16(pf[c2 * 32 + x4 + 2], pf[c2 * 32 + x4 + 3]);
+            pf[c2][x4 + e] = __float_as_uint(pv);
           }
-          // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
-          tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
+          pp[x4 >> 1] = pack_bf16(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1]));
+          pp[(x4 >> 1) + 1] =
+              pack_bf16(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3]));
         }
+        // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
+        tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
       }
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bar_p_ready);
 
-      // ---- dS^T = P^T (dP^T - Delta) -> swizzled [key][query] tile in smem.
+      // ---- dS^T = P^T (dP^T - Delta) -> swizzled [key][query] tile in smem,
+      // once TMA has read the previous tile's dQ staging (part A) from it.
       ok = warp_wait(&bar_dp_full, par, STT_DEVERR_BWD_WAIT);
+      if (ok && i > 0) ok = warp_wait(&bar_stg_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dd[2][16];
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t dp[32];
+        uint32_t dp[32], dd[16];
         tmem_ld32(tmem + lane_off + kColDP + half * 64 + c2 * 32, dp);
 #pragma unroll
         for (int x4 = 0; x4 < 32; x4 += 4) {
@@ -630,23 +676,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           float sv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            sv[e] = pf[c2 * 32 + x4 + e] * (__uint_as_float(dp[x4 + e]) - dv[e]);
-          dd[c2][x4 >> 1] = pack_bf16(sv[0], sv[1]);
-          dd[c2][(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
+            sv[e] = __uint_as_float(pf[c2][x4 + e]) * (__uint_as_float(dp[x4 + e]) - dv[e]);
+          dd[x4 >> 1] = pack_bf16(sv[0], sv[1]);
+          dd[(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
         }
-      }
-      // The dS^T buffer held the previous tile's dQ staging (part A) until
-      // TMA read it.
-      if (i > 0) {
-        ok = warp_wait(&bar_stg_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           *reinterpret_cast<uint4*>(sDS + swz_chunk_offset(r, half * 8 + c2 * 4 + w, kTile)) =
-              make_uint4(dd[c2][4 * w], dd[c2][4 * w + 1], dd[c2][4 * w + 2], dd[c2][4 * w + 3]);
+              make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(&bar_ds_ready);
@@ -659,39 +697,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         put_stat(par, stat_next);
         if (i + 3 < n_q) stat_next = fetch_stat(i + 3);
       }
-
-      // ---- dQ of this tile (rows = queries tq0 + r): read out of TMEM, then
-      // staged as [128 x 32] fp32 blocks for the producer's TMA reduce-add.
-      ok = warp_wait(&bar_dq_full, par, STT_DEVERR_BWD_WAIT);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t u[NP][32];
-      if constexpr (NP == 2)
-        tmem_ld32x2(tmem + lane_off + kColDP + half * 64, tmem + lane_off + kColDP + half * 64 + 32,
-                    u[0], u[NP - 1]);
-      else
-        tmem_ld32(tmem + lane_off + kColDP + half * 32, u[0]);
-      // dQ is out of TMEM: the MMA warp may overwrite the dP^T columns.
-      tc_fence_before();
-      warp_arrive(&bar_dq_free);
-      // Part B (the dO buffer, free since dV) first; part A (the dS^T buffer)
-      // once dK, its last reader, is done.
-#pragma unroll
-      for (int p = NP - 1; p >= 0; --p) {
-        if (p == 0) {
-          ok = warp_wait(&bar_dk_done, par, STT_DEVERR_BWD_WAIT);
-          if (!ok) break;
-        }
-        unsigned char* blk = dq_staging<D>(smem, p, st) + half * L::kStageBlkB;
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
-              P.scale * __uint_as_float(u[p][4 * w]), P.scale * __uint_as_float(u[p][4 * w + 1]),
-              P.scale * __uint_as_float(u[p][4 * w + 2]), P.scale * __uint_as_float(u[p][4 * w + 3]));
-      }
-      if (!ok) break;
-      fence_proxy_async_smem();
-      warp_arrive(&bar_stg_full);
     }
     if (ok && n_q > 0) {
       // dV and dK of this key tile into the block-0 gradients, summed over the
