@@ -285,33 +285,6 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
-// 16 lanes x 32 columns in the 16x256b shape, without waiting: thread t gets,
-// for j = 0..3, r[4j], r[4j+1] = lane (base + t/4), columns 8j + 2(t%4) + {0,1}
-// and r[4j+2], r[4j+3] = lane (base + 8 + t/4), the same columns, so four
-// consecutive threads hold 32 contiguous bytes of a row.  The values may be
-// used only after tmem_wait_ld_keep(r).
-#define STT_RW8(b) "+r"(r[b + 0]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), \
-                   "+r"(r[b + 4]), "+r"(r[b + 5]), "+r"(r[b + 6]), "+r"(r[b + 7])
-__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : STT_R8(0), STT_R8(8)
-      : "r"(taddr)
-      : "memory");
-}
-// Waits for this thread's TMEM loads; `r` passes through the statement so that
-// no use of the loaded registers is scheduled before the wait.
-__device__ __forceinline__ void tmem_wait_ld_keep(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : STT_RW8(0), STT_RW8(8) : : "memory");
-}
-
-// Relaxed gpu-scope vector add of two fp32 values to 8-byte aligned global memory.
-__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
-  asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b)
-               : "memory");
-}
-
 // Four 32-column loads (a0..a3 from ta, ta+32; b0..b3 from tb, tb+32), one wait.
 __device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t (&a0)[32],
                                             uint32_t (&a1)[32], uint32_t (&b0)[32],
