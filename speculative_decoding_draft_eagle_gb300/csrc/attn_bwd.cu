@@ -461,19 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idSS = idesc_bf16(128, kTile, false, false);  // S^T, dP^T
       const uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK (B MN-major)
       const uint32_t idQ = idesc_bf16(128, D, true, true);         // dQ (A, B MN-major)
-      const uint32_t aK = smem_u32(smem + L::k), aV = smem_u32(smem + L::v);
-      const uint32_t aDS = smem_u32(smem + L::ds);
+      // Base descriptors; each MMA only advances the start address.
+      const uint64_t kK = sdesc_sw128(smem_u32(smem + L::k), 16, 1024);     // K, K-major
+      const uint64_t kV = sdesc_sw128(smem_u32(smem + L::v), 16, 1024);     // V, K-major
+      const uint64_t mK = sdesc_sw128(smem_u32(smem + L::k), kTile * 128, 1024);  // K, MN-major
+      const uint64_t kQ0 = sdesc_sw128(smem_u32(smem + L::q0), 16, 1024);
+      const uint64_t mQ0 = sdesc_sw128(smem_u32(smem + L::q0), kTile * 128, 1024);
+      const uint64_t kDO0 = sdesc_sw128(smem_u32(smem + L::do0), 16, 1024);
+      const uint64_t mDO0 = sdesc_sw128(smem_u32(smem + L::do0), kTile * 128, 1024);
+      const uint64_t kDS = sdesc_sw128(smem_u32(smem + L::ds), 16, 1024);
+      const uint64_t mDS = sdesc_sw128(smem_u32(smem + L::ds), kTile * 128, 1024);
       // S^T(t) = K Q(t)^T into the S^T columns.
       auto issue_s = [&](int t) -> bool {
         const int s = t % NS;
         if (!mbar_wait(&bar_q_full[s], (uint32_t)(t / NS) & 1u, STT_DEVERR_BWD_WAIT)) return false;
         tc_fence_after();
-        const uint32_t aQ = smem_u32(smem + L::q0 + s * L::kTileB);
+        const uint64_t kQ = sdesc_add(kQ0, s * L::kTileB);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024),
-                       sdesc_sw128(aQ + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColS, sdesc_add(kK, off), sdesc_add(kQ, off), idSS, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bar_s_full);
         return true;
@@ -487,13 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && i > 0) ok = mbar_wait(&bar_dq_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t aQ = smem_u32(smem + L::q0 + st * L::kTileB);
-        const uint32_t aDO = smem_u32(smem + L::do0 + st * L::kTileB);
+        const uint64_t mQ = sdesc_add(mQ0, st * L::kTileB);
+        const uint64_t kDO = sdesc_add(kDO0, st * L::kTileB), mDO = sdesc_add(mDO0, st * L::kTileB);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aV + off, 16, 1024),
-                       sdesc_sw128(aDO + off, 16, 1024), idSS, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColDP, sdesc_add(kV, off), sdesc_add(kDO, off), idSS, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bar_dp_full);
         ok = mbar_wait(&bar_p_ready, par, STT_DEVERR_BWD_WAIT);
@@ -504,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           umma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                       sdesc_sw128(aDO + kk * 2048, kTile * 128, 1024), idKV,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+                       sdesc_add(mDO, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar_pt_free);
         if (i + 1 < n_q) {
           // P^T(i) consumed: S^T(i+1) may overwrite the S^T columns.
@@ -519,16 +524,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // B = K MN-major; into the dP^T columns.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + kColDP, sdesc_sw128(aDS + kk * 2048, kTile * 128, 1024),
-                       sdesc_sw128(aK + kk * 2048, kTile * 128, 1024), idQ, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColDP, sdesc_add(mDS, kk * 2048), sdesc_add(mK, kk * 2048), idQ,
+                       kk > 0 ? 1u : 0u);
         umma_commit(&bar_dq_full);
         // dK += dS^T Q: A = dS^T in smem (K-major over queries), B = Q MN-major.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + kColDK,
-                       sdesc_sw128(aDS + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024),
-                       sdesc_sw128(aQ + kk * 2048, kTile * 128, 1024), idKV,
-                       (i > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ss(tmem + kColDK, sdesc_add(kDS, (kk >> 2) * kTile * 128 + (kk & 3) * 32),
+                       sdesc_add(mQ, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar_q_empty[st]);
         umma_commit(&bar_dk_done);
       }

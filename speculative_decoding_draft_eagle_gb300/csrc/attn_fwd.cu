@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       const uint32_t idS = idesc_bf16(128, kTile, false, false);
       const uint32_t idO = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ);
+      // Base descriptors; each MMA only advances the start address.
+      const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::k0), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::v0), kTile * 128, 1024);
       bool ok = mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
       auto issue_pv = [&](int i) -> bool {
         const int st = i % kStages;
@@ -218,15 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bar_v_full[st], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT))
           return false;
         tc_fence_after();
-        const uint32_t aV = smem_u32(smem + L::v0 + st * L::kKV);
+        const uint64_t dV = sdesc_add(dV0, st * L::kKV);
         // A = P in TMEM: keys 64h.. of the tile live at column 64h of the S buffer.
         const uint32_t aP = tmem + kColS0 + (i & 1) * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(aV + kk * 2048, kTile * 128, 1024);
-          umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO,
-                       (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(dV, kk * 2048),
+                       idO, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar_o_done);
         umma_commit(&bar_v_empty[st]);
         return true;
@@ -239,12 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&bar_o_done, (uint32_t)(j - 2) & 1u, STT_DEVERR_FWD_WAIT);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t aK = smem_u32(smem + L::k0 + st * L::kKV);
+        const uint64_t dK = sdesc_add(dK0, st * L::kKV);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(aQ + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(aK + (kk >> 2) * kTile * 128 + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + kColS0 + sb * kTile, ad, bd, idS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
+          umma_bf16_ss(tmem + kColS0 + sb * kTile, sdesc_add(dQ, off), sdesc_add(dK, off), idS,
+                       kk > 0 ? 1u : 0u);
         }
         umma_commit(&bar_s_full[sb]);
         umma_commit(&bar_k_empty[st]);

@@ -239,6 +239,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor with its start address advanced by `bytes` (a multiple
+// of 16): the 14-bit start field holds shared-memory addresses >> 4, which
+// stay below 2^14 for any address inside shared memory, so the add never
+// carries out of the low word.  One integer add per MMA in the issue loops.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = (uint32_t)d + (bytes >> 4), hi = (uint32_t)(d >> 32);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 // TMEM loads, 32 lanes x 32-bit, N consecutive columns per thread; the wait is
 // folded into the same asm statement so no use of the registers can be
 // scheduled before the data has arrived.
