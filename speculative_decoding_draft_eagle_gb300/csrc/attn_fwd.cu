@@ -15,7 +15,7 @@
 //     The online softmax is order independent, so taking the suffix keys last
 //     gives the same result as any other order.
 //
-// Warp roles (320 threads, one CTA per 128-row query tile of one head):
+// Warp roles (352 threads, one CTA per 128-row query tile of one head):
 //   warps 0-7  softmax: warps w and w+4 own the 32 query rows of TMEM lane
 //              quarter w%4 and split the 128 key columns (and O's D columns)
 //              in halves; the row max is exchanged through shared memory.
@@ -25,9 +25,11 @@
 //              keys and O / lse.
 //   warp 8     TMA producer (one lane): Q once, then K/V tiles (2 stages),
 //              then the suffix K_j / V_j tiles through the same buffers.
-//   warp 9     MMA issuer (one lane): S(j) into one of two TMEM buffers, then
-//              O += P(j-1) V(j-1) with P read from TMEM, so S(j+1) overlaps the
-//              softmax of tile j.
+//   warp 9     S issuer (one lane): S(j) into TMEM buffer j % 3 as soon as
+//              K(j) is in and O += P(j-3) V has read the buffer.
+//   warp 10    P V issuer (one lane): O += P(j) V(j), P read from TMEM.  Two
+//              issuing threads, because one thread's issue, commit and wait
+//              latencies per key tile exceed the tensor cores' time for it.
 #include "../../include/stt.h"
 #include "attn_common.cuh"
 
@@ -35,10 +37,10 @@ namespace stt {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmax = 256;
 constexpr int kSoftmaxWarps = kSoftmax / 32;  // barriers count one arrival per warp
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
 
 struct FwdParams {
@@ -66,10 +68,12 @@ struct FwdSmem {
   static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
 };
 
-// TMEM columns: S buffers at 0 and 128 (P of column half h is written back
-// into columns [64h, 64h + 32) of its S buffer), O at 256.
+// TMEM columns: S buffers at 0, 128 and 256 (P of column half h is written
+// back into columns [64h, 64h + 32) of its S buffer), O at 384.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColO = 256;
+constexpr int kSBufs = 3;
+constexpr uint32_t kColS0 = 0, kColO = kSBufs * kTile;
+static_assert(kColO + 128 <= kTmemCols, "three S buffers and O fit in TMEM");
 
 // Dot product of row r of two swizzled [128 x D] bf16 tiles in shared memory.
 template <int D>
@@ -101,9 +105,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // s_full / s_free per S buffer (S(j) uses buffer j % 3); p_full alternates
+  // by tile parity so that a waiter can never miss a phase; o_done counts
+  // every O += P V.
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
-      bar_v_empty[kStages], bar_s_full[2], bar_p_full, bar_o_done, bar_drain,
-      bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
+      bar_v_empty[kStages], bar_s_full[kSBufs], bar_s_free[kSBufs], bar_p_full[2], bar_o_done,
+      bar_drain, bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
   __shared__ float s_sum[2][kTile];     // [half][row] partial row sum
@@ -129,10 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_sfx_full[s], 1);
       mbar_init(&bar_sfx_empty[s], kSoftmaxWarps);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&bar_s_full[s], 1);
-    mbar_init(&bar_p_full, kSoftmaxWarps);
+    for (int s = 0; s < kSBufs; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_s_free[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_p_full[s], kSoftmaxWarps);
     mbar_init(&bar_o_done, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kSoftmaxWarps);
     fence_mbar_init();
   }
@@ -205,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = (issued_s > kStages ? issued_s - kStages : 0); i < issued_s; ++i)
           mbar_wait(&bar_sfx_full[i % kStages], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT);
     }
-  } else if (warp == kWarpMma) {
-    // -------------------------------------------------------- MMA issuer --
+  } else if (warp == kWarpMma || warp == kWarpPv) {
+    // ------------------------------------------------------- MMA issuers --
     if (lane == 0 && n_kv > 0) {
       const uint32_t idS = idesc_bf16(128, kTile, false, false);
       const uint32_t idO = idesc_bf16(128, D, false, true);
@@ -214,45 +224,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + L::k0), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + L::v0), kTile * 128, 1024);
-      bool ok = mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % kStages;
-        if (!mbar_wait(&bar_p_full, (uint32_t)i & 1u, STT_DEVERR_FWD_WAIT)) return false;
-        if (!mbar_wait(&bar_v_full[st], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT))
-          return false;
-        tc_fence_after();
-        const uint64_t dV = sdesc_add(dV0, st * L::kKV);
-        // A = P in TMEM: keys 64h.. of the tile live at column 64h of the S buffer.
-        const uint32_t aP = tmem + kColS0 + (i & 1) * kTile;
+      bool ok = true;
+      if (warp == kWarpMma) {
+        // S(j) = Q K_j^T into buffer j % 3 once O += P(j-3) V has read it.
+        ok = mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int st = j % kStages, sb = j % kSBufs;
+          ok = mbar_wait(&bar_k_full[st], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+          if (ok && j >= kSBufs)
+            ok = mbar_wait(&bar_s_free[sb], (uint32_t)(j / kSBufs - 1) & 1u, STT_DEVERR_FWD_WAIT);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dK = sdesc_add(dK0, st * L::kKV);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(dV, kk * 2048),
-                       idO, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar_o_done);
-        umma_commit(&bar_v_empty[st]);
-        return true;
-      };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % kStages, sb = j & 1;
-        ok = mbar_wait(&bar_k_full[st], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
-        // S buffer sb holds P(j-2) until O += P(j-2) V(j-2) has completed.
-        if (ok && j >= 2)
-          ok = mbar_wait(&bar_o_done, (uint32_t)(j - 2) & 1u, STT_DEVERR_FWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t dK = sdesc_add(dK0, st * L::kKV);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS0 + sb * kTile, sdesc_add(dQ, off), sdesc_add(dK, off), idS,
-                       kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColS0 + sb * kTile, sdesc_add(dQ, off), sdesc_add(dK, off), idS,
+                         kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bar_s_full[sb]);
+          umma_commit(&bar_k_empty[st]);
         }
-        umma_commit(&bar_s_full[sb]);
-        umma_commit(&bar_k_empty[st]);
-        if (j >= 1) ok = issue_pv(j - 1);
+      } else {
+        // O += P(i) V(i): A = P in TMEM (keys 64h.. of the tile live at column
+        // 64h of its S buffer), B = V MN-major.
+        for (int i = 0; ok && i < n_kv; ++i) {
+          const int st = i % kStages, sb = i % kSBufs;
+          ok = mbar_wait(&bar_p_full[i & 1], (uint32_t)(i >> 1) & 1u, STT_DEVERR_FWD_WAIT) &&
+               mbar_wait(&bar_v_full[st], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dV = sdesc_add(dV0, st * L::kKV);
+          const uint32_t aP = tmem + kColS0 + sb * kTile;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(dV, kk * 2048),
+                         idO, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_o_done);
+          umma_commit(&bar_s_free[sb]);
+          umma_commit(&bar_v_empty[st]);
+        }
       }
-      if (ok) ok = issue_pv(n_kv - 1);
-      // Every MMA issued by this thread is complete before TMEM or the stage
+      // Every MMA issued by either thread is complete before TMEM or the stage
       // buffers are reused.
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_FWD_WAIT);
@@ -270,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int sb = j & 1;
-      ok = warp_wait(&bar_s_full[sb], (uint32_t)(j >> 1) & 1u, STT_DEVERR_FWD_WAIT);
+      const int sb = j % kSBufs;
+      ok = warp_wait(&bar_s_full[sb], (uint32_t)(j / kSBufs) & 1u, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[2][32];
@@ -300,10 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
       // Combine the two halves' maxima (buffer double-buffered by tile parity).
-      s_max[sb][half][r] = mt;
+      s_max[j & 1][half][r] = mt;
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
-      mt = fmaxf(mt, s_max[sb][half ^ 1][r]);
+      mt = fmaxf(mt, s_max[j & 1][half ^ 1][r]);
 
       float alpha = 1.f;
       bool rescale_o = false;
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      warp_arrive(&bar_p_full);
+      warp_arrive(&bar_p_full[j & 1]);
     }
     if (ok && n_kv > 0) {
       ok = warp_wait(&bar_o_done, (uint32_t)(n_kv - 1) & 1u, STT_DEVERR_FWD_WAIT);
