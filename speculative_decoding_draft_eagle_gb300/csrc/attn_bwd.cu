@@ -34,10 +34,11 @@
 namespace stt {
 namespace {
 
-constexpr int kThreads = 448;   // warps 0-7 compute, 8 TMA, 9 MMA, 10-13 dQ epilogue
+// warps 0-7 compute, 8 TMA, 9 and 14 MMA issue, 10-13 dQ epilogue
+constexpr int kThreads = 480;
 constexpr int kCompute = 256;
 constexpr int kComputeWarps = kCompute / 32;  // barriers count one arrival per warp
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10;
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpMma2 = 14;
 constexpr int kEpiWarps = 4;  // one per TMEM lane quarter (warp % 4)
 
 struct BwdParams {
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_stg_full, kEpiWarps);
     mbar_init(&bar_stg_free, 1);
     mbar_init(&bar_final, 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kComputeWarps);
     fence_mbar_init();
   }
@@ -451,12 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bulk_wait_group0();
     }
-  } else if (warp == kWarpMma) {
-    // -------------------------------------------------------- MMA issuer --
-    // Per query tile i: dP^T(i) once dQ(i-1) is out of TMEM, dV(i) once P^T(i)
-    // is in TMEM, S^T(i+1) as soon as dV(i) has consumed P^T(i) (it runs while
-    // the compute warps form dS(i)), then dQ(i) and dK(i) once dS^T(i) is in
-    // shared memory (dQ first: its read-out overlaps dK).
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
+    // ------------------------------------------------------- MMA issuers --
+    // Two issuing threads, because one thread's issue, commit and wait
+    // latencies for the five products of a tile exceed the tensor cores' time.
+    //   warp 9:  S^T(i) once dV(i-1) has consumed P^T(i-1) from the S^T
+    //            columns; dP^T(i) once dQ(i-1) is out of the dP^T columns.
+    //   warp 14: dV(i) once P^T(i) is in TMEM; dQ(i) then dK(i) once dS^T(i)
+    //            is in shared memory (dQ first: its read-out overlaps dK).
+    // Each commit's mbarrier fires when every MMA issued before it by the
+    // committing thread is complete.
     if (lane == 0 && n_q > 0) {
       const uint32_t idSS = idesc_bf16(128, kTile, false, false);  // S^T, dP^T
       const uint32_t idKV = idesc_bf16(128, D, false, true);       // dV, dK (B MN-major)
@@ -471,72 +476,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t mDO0 = sdesc_sw128(smem_u32(smem + L::do0), kTile * 128, 1024);
       const uint64_t kDS = sdesc_sw128(smem_u32(smem + L::ds), 16, 1024);
       const uint64_t mDS = sdesc_sw128(smem_u32(smem + L::ds), kTile * 128, 1024);
-      // S^T(t) = K Q(t)^T into the S^T columns.
-      auto issue_s = [&](int t) -> bool {
-        const int s = t % NS;
-        if (!mbar_wait(&bar_q_full[s], (uint32_t)(t / NS) & 1u, STT_DEVERR_BWD_WAIT)) return false;
-        tc_fence_after();
-        const uint64_t kQ = sdesc_add(kQ0, s * L::kTileB);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColS, sdesc_add(kK, off), sdesc_add(kQ, off), idSS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&bar_s_full);
-        return true;
-      };
-      bool ok = mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT) && issue_s(0);
-      for (int i = 0; ok && i < n_q; ++i) {
-        const int st = i % NS;
-        const uint32_t par = (uint32_t)i & 1u;
-        ok = mbar_wait(&bar_do_full[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
-        // dQ(i-1) has been read out of the dP^T columns.
-        if (ok && i > 0) ok = mbar_wait(&bar_dq_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t mQ = sdesc_add(mQ0, st * L::kTileB);
-        const uint64_t kDO = sdesc_add(kDO0, st * L::kTileB), mDO = sdesc_add(mDO0, st * L::kTileB);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
-          umma_bf16_ss(tmem + kColDP, sdesc_add(kV, off), sdesc_add(kDO, off), idSS, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&bar_dp_full);
-        ok = mbar_wait(&bar_p_ready, par, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO: A = P^T in TMEM (8 columns per 16 queries; queries
-        // 64h.. live at column 64h), B = dO MN-major.
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                       sdesc_add(mDO, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar_pt_free);
-        if (i + 1 < n_q) {
-          // P^T(i) consumed: S^T(i+1) may overwrite the S^T columns.
-          ok = mbar_wait(&bar_pt_free, par, STT_DEVERR_BWD_WAIT) && issue_s(i + 1);
+      bool ok = true;
+      if (warp == kWarpMma) {
+        ok = mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
+        for (int i = 0; ok && i < n_q; ++i) {
+          const int st = i % NS;
+          const uint32_t ph = (uint32_t)(i / NS) & 1u, prev = (uint32_t)(i - 1) & 1u;
+          ok = mbar_wait(&bar_q_full[st], ph, STT_DEVERR_BWD_WAIT);
+          if (ok && i > 0) ok = mbar_wait(&bar_pt_free, prev, STT_DEVERR_BWD_WAIT);
           if (!ok) break;
+          tc_fence_after();
+          const uint64_t kQ = sdesc_add(kQ0, st * L::kTileB);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColS, sdesc_add(kK, off), sdesc_add(kQ, off), idSS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bar_s_full);
+          ok = mbar_wait(&bar_do_full[st], ph, STT_DEVERR_BWD_WAIT);
+          if (ok && i > 0) ok = mbar_wait(&bar_dq_free, prev, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kDO = sdesc_add(kDO0, st * L::kTileB);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kTile * 128 + (kk & 3) * 32;
+            umma_bf16_ss(tmem + kColDP, sdesc_add(kV, off), sdesc_add(kDO, off), idSS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bar_dp_full);
         }
-        ok = mbar_wait(&bar_ds_ready, par, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ = dS K: A = the dS^T tile read MN-major (rows = keys = K dim),
-        // B = K MN-major; into the dP^T columns.
+      } else {
+        for (int i = 0; ok && i < n_q; ++i) {
+          const int st = i % NS;
+          const uint32_t par = (uint32_t)i & 1u;
+          // dV(i) reads dO(i): its load is waited for here too, since P^T(i)
+          // can be ready before dP^T(i) (the other thread's wait) is issued.
+          ok = mbar_wait(&bar_do_full[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT) &&
+               mbar_wait(&bar_p_ready, par, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t mQ = sdesc_add(mQ0, st * L::kTileB), mDO = sdesc_add(mDO0, st * L::kTileB);
+          // dV += P^T dO: A = P^T in TMEM (8 columns per 16 queries; queries
+          // 64h.. live at column 64h), B = dO MN-major.
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + kColDP, sdesc_add(mDS, kk * 2048), sdesc_add(mK, kk * 2048), idQ,
-                       kk > 0 ? 1u : 0u);
-        umma_commit(&bar_dq_full);
-        // dK += dS^T Q: A = dS^T in smem (K-major over queries), B = Q MN-major.
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_ts(tmem + kColDV, tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                         sdesc_add(mDO, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_pt_free);
+          ok = mbar_wait(&bar_ds_ready, par, STT_DEVERR_BWD_WAIT);
+          if (!ok) break;
+          tc_fence_after();
+          // dQ = dS K: A = the dS^T tile read MN-major (rows = keys = K dim),
+          // B = K MN-major; into the dP^T columns.
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_ss(tmem + kColDK, sdesc_add(kDS, (kk >> 2) * kTile * 128 + (kk & 3) * 32),
-                       sdesc_add(mQ, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar_q_empty[st]);
-        umma_commit(&bar_dk_done);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_ss(tmem + kColDP, sdesc_add(mDS, kk * 2048), sdesc_add(mK, kk * 2048), idQ,
+                         kk > 0 ? 1u : 0u);
+          umma_commit(&bar_dq_full);
+          // dK += dS^T Q: A = dS^T in smem (K-major over queries), B = Q MN-major.
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_ss(tmem + kColDK, sdesc_add(kDS, (kk >> 2) * kTile * 128 + (kk & 3) * 32),
+                         sdesc_add(mQ, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_q_empty[st]);
+          umma_commit(&bar_dk_done);
+        }
+        // The last dK also follows every S^T / dP^T product of the tile loop
+        // (the compute warps consumed them before dS^T was ready).
+        if (ok) umma_commit(&bar_final);
       }
-      if (ok) umma_commit(&bar_final);
-      // Every MMA issued by this thread is complete before TMEM is released.
+      // Every MMA issued by either thread is complete before TMEM is released.
       umma_commit(&bar_drain);
       mbar_wait(&bar_drain, 0, STT_DEVERR_BWD_WAIT);
     }
