@@ -267,10 +267,11 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 // Shared memory: K and V of the key tile, two stages of Q and dO, the dS^T
 // tile.  A query tile's dQ leaves through fp32 staging blocks of [128 x 32]
-// (16 KB; block h holds 32 columns of compute half h): part A in the dS^T
-// buffer (free once dK and dQ of the tile are done; TMA reads it first, so it
-// is free again before the next dS^T), and for D = 128 part B in the tile's dO
-// buffer (free once dV is done; reloaded only after TMA has read it).
+// (16 KB; block h holds 32 columns of compute half h) in the tile's own Q and
+// dO buffers, free once dK (Q's last reader) and dV (dO's) are done: part A in
+// the Q buffer, and for D = 128 part B in the dO buffer (for D = 64 part A's
+// second block).  The next tiles' Q and dO are loaded into them once TMA has
+// read the staging.
 template <int D>
 struct CausalSmem {
   static constexpr int kTileB = kTile * D * 2;  // one 128 x D bf16 tile
@@ -285,18 +286,20 @@ struct CausalSmem {
   static constexpr int ds = do0 + kStages * kTileB;
   static constexpr int total = ds + kDsB;
   static constexpr int alloc = total;  // the dynamic array is declared 1024-byte aligned
-  static_assert(2 * kStageBlkB == kDsB, "staging part A fills the dS^T buffer");
-  static_assert(D == 64 || 2 * kStageBlkB == kTileB, "staging part B fills one dO buffer");
+  static_assert(D == 64 ? kStageBlkB == kTileB : 2 * kStageBlkB == kTileB,
+                "a dQ staging part fills one Q or dO buffer");
   // The final dK / dV staging (2 x D/32 blocks) overwrites K, V and the Q
-  // stages only, never a buffer the last dQ reduction may still read.
+  // stages, once TMA has read every dQ staging.
   static_assert(2 * (D / 32) * kStageBlkB <= do0, "dK/dV staging must stay below the dO stages");
 };
 
-// Staging part p (0: dS^T buffer, 1: dO buffer of stage st).
+// Staging block hh of part p of stage st: dQ columns [hh D/2 + 32 p, +32).
 template <int D>
-__device__ __forceinline__ unsigned char* dq_staging(unsigned char* smem, int p, int st) {
+__device__ __forceinline__ unsigned char* dq_staging(unsigned char* smem, int p, int hh, int st) {
   using L = CausalSmem<D>;
-  return p == 0 ? smem + L::ds : smem + L::do0 + st * L::kTileB;
+  const int q = L::q0 + st * L::kTileB, o = L::do0 + st * L::kTileB;
+  if constexpr (D == 64) return smem + (hh == 0 ? q : o);
+  return smem + (p == 0 ? q : o) + hh * L::kStageBlkB;
 }
 
 template <int D>
@@ -320,14 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) record_error(STT_DEVERR_SMEM_ALIGN);
     return;
   }
-  // Producer -> MMA: kv, q_full, do_full.  MMA -> producer: q_empty.
-  // MMA -> compute: s_full, dp_full, final.  Compute -> MMA: p_ready,
-  // ds_ready.  MMA -> epilogue: dq_full, dk_done.  Epilogue -> MMA: dq_free.
-  // Epilogue -> producer: stg_full; producer -> compute: stg_free (staging
-  // part A read).  MMA -> itself: pt_free, drain.  Compute group: grp.
-  __shared__ uint64_t bar_kv, bar_q_full[NS], bar_do_full[NS], bar_q_empty[NS], bar_s_full,
+  // Producer -> MMA: kv, q_full, do_full.  MMA -> compute: s_full, dp_full,
+  // dk_done, final.  Compute -> MMA: p_ready, ds_ready.  MMA -> epilogue:
+  // dq_full, dk_done.  Epilogue -> MMA: dq_free.  Epilogue -> producer:
+  // stg_full.  MMA -> MMA: pt_free.  Issuers: drain.  Compute group: grp.
+  __shared__ uint64_t bar_kv, bar_q_full[NS], bar_do_full[NS], bar_s_full,
       bar_dp_full, bar_p_ready, bar_pt_free, bar_ds_ready, bar_dq_full, bar_dk_done, bar_dq_free,
-      bar_stg_full, bar_stg_free, bar_final, bar_drain, bar_grp;
+      bar_stg_full, bar_stg_done, bar_final, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
   // [tile parity][lse2 | Delta][query]: tile i's statistics sit in buffer i & 1.
   __shared__ __align__(16) float s_stat[2][2][kTile];
@@ -347,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_q_full[s], 1);
       mbar_init(&bar_do_full[s], 1);
-      mbar_init(&bar_q_empty[s], 1);
     }
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_dp_full, 1);
@@ -358,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_dk_done, 1);
     mbar_init(&bar_dq_free, kEpiWarps);
     mbar_init(&bar_stg_full, kEpiWarps);
-    mbar_init(&bar_stg_free, 1);
     mbar_init(&bar_final, 1);
+    mbar_init(&bar_stg_done, 1);  // producer: every dQ staging read by TMA
     mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kComputeWarps);
     fence_mbar_init();
@@ -411,37 +412,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % NS;
         const int tq0 = (t_first + i) * kTile;
-        // Q(i) is free once dK(i) is done, before the staging of part A; its
-        // successor is loaded first, ahead of the reductions in TMA's queue.
         const bool more = i + NS < n_q;
+        // dQ of tile i, staged in its Q and dO buffers (dK(i) and dV(i) done).
+        ok = mbar_wait(&bar_stg_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+        if (!ok) break;
+        // Part A first; Q(i + NS) follows as soon as TMA has read it, ahead of
+        // part B in TMA's queue, since S^T(i + NS) needs it first.
+        for (int hh = 0; hh < 2; ++hh)
+          tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 0, hh, st), hh * (D / 2), tq0, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
         if (more) {
-          ok = mbar_wait(&bar_q_empty[st], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
-          if (!ok) break;
           load_q(i + NS);
           ++issued_q;
         }
-        // dQ of tile i: part p, block hh holds columns [hh D/2 + 32 p, +32).
-        ok = mbar_wait(&bar_stg_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
-        if (!ok) break;
-        for (int p = 0; p < NP; ++p) {
-          unsigned char* sb = dq_staging<D>(smem, p, st);
+        if constexpr (NP == 2) {
           for (int hh = 0; hh < 2; ++hh)
-            tma_reduce_add_3d(&tmDQ, sb + hh * L::kStageBlkB, hh * (D / 2) + 32 * p, tq0, bh);
+            tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 1, hh, st), hh * (D / 2) + 32, tq0, bh);
           bulk_commit_group();
+          bulk_wait_group_read0();
         }
-        // Part A read: the compute warps may write the next dS^T.
-        if constexpr (NP == 2)
-          bulk_wait_group_read1();
-        else
-          bulk_wait_group_read0();
-        mbar_arrive(&bar_stg_free);
         if (more) {
-          // Part B read: dO(i)'s buffer takes dO(i + NS).
-          bulk_wait_group_read0();
           load_do(i + NS);
           ++issued_do;
         }
       }
+      // The compute warps' final dK / dV staging reuses the Q buffers.
+      if (ok) mbar_arrive(&bar_stg_done);
       if (!ok) {
         // Gave up: let every copy already issued land before the CTA exits.
         mbar_wait(&bar_kv, 0, STT_DEVERR_BWD_WAIT);
@@ -538,7 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_bf16_ss(tmem + kColDK, sdesc_add(kDS, (kk >> 2) * kTile * 128 + (kk & 3) * 32),
                          sdesc_add(mQ, kk * 2048), idKV, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_q_empty[st]);
           umma_commit(&bar_dk_done);
         }
         // The last dK also follows every S^T / dP^T product of the tile loop
@@ -554,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Thread = query row r of TMEM lane quarter warp % 4.  Per tile: the
     // columns of staging part B (the dO buffer, free since dV) go first, then
     // the part A columns are read into registers, TMEM is released to dP^T of
-    // the next tile, and part A (the dS^T buffer) is written once dK, its last
+    // the next tile, and part A (the Q buffer) is written once dK, its last
     // reader, is done.  Staging part p, block hh holds dQ columns
     // [hh D/2 + 32 p, +32) of all 128 rows.
     const int quarter = warp & 3;
@@ -575,11 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if constexpr (NP == 2) {
+        // Part B into the dO buffer (dV, its last reader, is done).
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t u[32];
           tmem_ld32(tmem + lane_off + kColDP + hh * (D / 2) + 32, u);
-          stage(dq_staging<D>(smem, 1, st) + hh * L::kStageBlkB, u);
+          stage(dq_staging<D>(smem, 1, hh, st), u);
         }
       }
       uint32_t a0[32], a1[32];
@@ -589,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bar_dq_free);
       ok = warp_wait(&bar_dk_done, par, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
-      stage(dq_staging<D>(smem, 0, st), a0);
-      stage(dq_staging<D>(smem, 0, st) + L::kStageBlkB, a1);
+      stage(dq_staging<D>(smem, 0, 0, st), a0);
+      stage(dq_staging<D>(smem, 0, 1, st), a1);
       fence_proxy_async_smem();
       warp_arrive(&bar_stg_full);
     }
@@ -672,9 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bar_p_ready);
 
       // ---- dS^T = P^T (dP^T - Delta) -> swizzled [key][query] tile in smem,
-      // once TMA has read the previous tile's dQ staging (part A) from it.
+      // once dQ(i-1) and dK(i-1), the previous tile's readers, are done (the
+      // other issuing thread commits dk_done after both).
       ok = warp_wait(&bar_dp_full, par, STT_DEVERR_BWD_WAIT);
-      if (ok && i > 0) ok = warp_wait(&bar_stg_free, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
+      if (ok && i > 0) ok = warp_wait(&bar_dk_done, (uint32_t)(i - 1) & 1u, STT_DEVERR_BWD_WAIT);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -712,12 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && n_q > 0) {
       // dV and dK of this key tile into the block-0 gradients, summed over the
-      // group's query heads: every MMA is done, so K, V and the Q stages are
-      // free and all D/32 chunks of both are staged at once (below the dO
-      // stages and the dS^T buffer, which the last dQ reduction may still
-      // read) and reduce-added by TMA (rows kv >= T hold zeros; rows past
-      // Q_LEN are clipped).
-      ok = warp_wait(&bar_final, 0, STT_DEVERR_BWD_WAIT);
+      // group's query heads: once every MMA is done and TMA has read every dQ
+      // staging, K, V and the Q stages are free and all D/32 chunks of both
+      // are staged at once and reduce-added by TMA (rows kv >= T hold zeros;
+      // rows past Q_LEN are clipped).
+      ok = warp_wait(&bar_final, 0, STT_DEVERR_BWD_WAIT) &&
+           warp_wait(&bar_stg_done, 0, STT_DEVERR_BWD_WAIT);
       if (ok) {
         tc_fence_after();
 #pragma unroll
