@@ -14,6 +14,8 @@ struct CePlan {
   int C;         // CTAs per row (thread-block cluster size)
   int slice;     // elements of a row per CTA
   int smem;      // dynamic shared memory bytes per CTA
+  bool persistent;  // persistent clusters walking the rows, nb row buffers per CTA
+  int nb;
 };
 CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V);
 constexpr int64_t kCeMaxV = 409600;  // 16 CTAs x 25600 elements

@@ -13,11 +13,15 @@
 //   * Each CTA reduces its slice to (max, sum exp, Sp, Spz); the C partials are
 //     exchanged through distributed shared memory and combined with the usual
 //     max-rescaling, so every CTA knows the row's lse.
-//   * The gradient is computed from the shared-memory copy and streamed out with
-//     coalesced 16-byte stores.  Rows with g = 0 are never read: their gradient
-//     is exactly zero and is written directly.
+//   * The gradient is streamed out with coalesced 16-byte stores.  Rows with
+//     g = 0 are never read: their gradient is exactly zero and is written
+//     directly.
 //   * Per-row weighted losses g_r * loss_r go to the workspace; a one-CTA kernel
 //     sums them in a fixed order, so the scalar loss is deterministic.
+// Two kernels implement this.  soft_ce_persistent_kernel (16-byte aligned rows,
+// slices of at most kPSliceMax elements) keeps one cluster per group of SMs
+// resident and pipelines rows through it; soft_ce_kernel (any row, one cluster
+// per row) covers the rest.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -245,6 +249,291 @@ __global__ void __launch_bounds__(kThreads) soft_ce_kernel(const CeParams P) {
   if (C > 1) cluster_wait_acquire();
 }
 
+// ---------------------------------------------------------------------------
+// Persistent variant (bulk path, V up to kPSliceMax * kMaxCluster).
+//
+// A cluster of C CTAs (one per SM) walks the rows cid, cid + ncl, ... where
+// ncl is the number of co-resident clusters.  Each CTA owns one slice of every
+// row.  A producer warp streams the CTA's slices of the cluster's rows with
+// g != 0 into nb shared-memory buffers (z slice, p slice) with bulk copies, as
+// far ahead as the buffers allow; kPWarps consumer warps process them.
+//
+// The consumers are software-pipelined over the exchange of partial
+// statistics.  In iteration v (the v-th row with g != 0) each consumer warp
+// runs
+//   reduce(v)   copy its part of the slice (at most kPVec float4 of z and of p
+//               per thread) into registers and release the buffer; reduce it
+//               to (max m_w, sum e, Sp, Spz) with e = exp(z - m_w) kept in
+//               registers; lane r pushes this warp partial into slot
+//               [v & 3][rank * kPWarps + warp] of CTA r with st.async, which
+//               counts 16 bytes on CTA r's mbarrier xbar[v & 3];
+//   finish(v-1) wait until xbar[(v-1) & 3] has seen the C * kPWarps partials
+//               of row v-1, fold them into lse, and write the gradient
+//               e exp(m_w - lse) g Sp - p g of row v-1 from the registers kept
+//               for it.
+// The exchange of row v-1 has all of reduce(v) to land in, and no block-wide
+// or cluster-wide barrier sits in the loop (the release of a cluster barrier
+// would also wait for the CTA's global stores to drain).
+// Slot and mbarrier reuse: a warp pushes row v + 4 after its finish(v + 2),
+// which needed the push of row v + 2 by every warp of every CTA; each warp
+// makes that push after its own finish(v).  So all readers of a slot (and all
+// waiters on its phase) are done before the slot is written again.
+// Masked rows take no buffer and no exchange: all CTAs of a cluster see the
+// same g and write zeros.
+constexpr int kPWarps = 8;                     // consumer warps
+constexpr int kPThreads = (kPWarps + 1) * 32;  // + the producer warp
+constexpr int kPConsumers = kPWarps * 32;
+constexpr int kPVec = 7;                  // float4 of z (and of p) per consumer thread at most
+constexpr int kPSliceTarget = 7168;       // preferred elements per CTA
+// Two row buffers: more let the producer run further ahead but measured
+// slower (5.1 vs 5.8 TB/s with three), so the smaller shared footprint wins.
+constexpr int kPMinBufs = 2;
+constexpr int kPMaxBufs = 2;
+constexpr int kPSmemBudget = 200 * 1024;  // shared bytes for the row buffers
+constexpr int kPSliceMax = kPConsumers * kPVec * 4;
+constexpr int kPParts = kMaxCluster * kPWarps;  // warp partials of one row, at most
+static_assert(kPSliceMax * 8 * kPMinBufs <= kPSmemBudget, "buffers for the largest slice");
+
+struct CePParams {
+  float* z;
+  const float* p;
+  const float* g;
+  float* row_loss;
+  float* wl;
+  long long N, V;
+  int C;
+  int slice;
+  int nb;
+};
+
+// One row's slice as a consumer thread keeps it between reduce and finish.
+struct CeRowRegs {
+  float4 e[kPVec];  // exp(z - m_w)
+  float4 p[kPVec];
+  long long row;
+  float g;
+  float m;          // the warp's max m_w
+};
+
+__global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const CePParams P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ uint64_t full[kPMaxBufs];
+  __shared__ uint64_t empty[kPMaxBufs];
+  __shared__ uint64_t xbar[4];
+  __shared__ __align__(16) float4 stats[4][kPParts];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = P.C;
+  const uint32_t rank = cluster_ctarank();
+  const long long ncl = gridDim.x / C;
+  const long long cid = blockIdx.x / C;
+  const long long begin = (long long)rank * P.slice;
+  const long long rem = P.V - begin;
+  const int len = rem <= 0 ? 0 : (rem < P.slice ? (int)rem : P.slice);
+  const int n4 = len >> 2;
+  const int nb = P.nb;
+  float* const sbase = reinterpret_cast<float*>(smem_raw);
+
+  if (tid == 0) {
+    for (int b = 0; b < nb; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], kPWarps);
+    }
+    for (int k = 0; k < 4; ++k) mbar_init(&xbar[k], 1);
+    fence_mbar_init();
+  }
+  // Every CTA's mbarriers are initialised before any CTA pushes to them.
+  cluster_arrive_release();
+  cluster_wait_acquire();
+
+  if (warp == kPWarps) {
+    // Producer: the slices of the cluster's rows with g != 0, in order.
+    if (lane == 0 && len > 0) {
+      int j = 0;
+      float gr = cid < P.N ? __ldg(P.g + cid) : 0.0f;
+      for (long long r = cid; r < P.N; r += ncl) {
+        const float gcur = gr;
+        if (r + ncl < P.N) gr = __ldg(P.g + r + ncl);
+        if (gcur == 0.0f) continue;
+        const int b = j % nb;
+        if (j >= nb) mbar_wait(&empty[b], (uint32_t)(j / nb - 1) & 1u, STT_DEVERR_CE_WAIT);
+        float* zs = sbase + (size_t)b * 2 * P.slice;
+        const float* zsrc = P.z + r * P.V + begin;
+        const float* psrc = P.p + r * P.V + begin;
+        mbar_arrive_expect_tx(&full[b], 8u * (uint32_t)len);
+        for (int c = 0; c < len; c += kChunk) {
+          const uint32_t bytes = (uint32_t)min(kChunk, len - c) * 4u;
+          bulk_load(zs + c, zsrc + c, bytes, &full[b]);
+          bulk_load(zs + P.slice + c, psrc + c, bytes, &full[b]);
+        }
+        ++j;
+      }
+    }
+    __syncwarp();
+  } else {
+    // Consumers.
+    CeRowRegs ra, rb;
+    long long row = cid;
+    float g_row = cid < P.N ? __ldg(P.g + cid) : 0.0f;
+    int v = 0;  // valid rows reduced so far
+
+    // Moves `row` to the cluster's next row with g != 0, writing zeros (and
+    // zero losses) for the masked rows passed on the way.  False at the end.
+    auto next_valid = [&]() -> bool {
+      while (row < P.N && g_row == 0.0f) {
+        float* zrow = P.z + row * P.V + begin;
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kPVec; ++k) {
+          const int i = tid + k * kPConsumers;
+          if (i < n4) st_global_cs_f4(zrow + 4 * i, zero);
+        }
+        if (rank == 0 && tid == 0) {
+          if (P.row_loss) P.row_loss[row] = 0.0f;
+          P.wl[row] = 0.0f;
+        }
+        row += ncl;
+        g_row = row < P.N ? __ldg(P.g + row) : 0.0f;
+      }
+      return row < P.N;
+    };
+
+    // reduce(v) of the current row into `cur`, then push the warp partial.
+    auto reduce = [&](CeRowRegs& cur) {
+      const int b = v % nb;
+      const float4* zs4 = reinterpret_cast<const float4*>(sbase + (size_t)b * 2 * P.slice);
+      const float4* ps4 = reinterpret_cast<const float4*>(sbase + (size_t)b * 2 * P.slice + P.slice);
+      cur.row = row;
+      cur.g = g_row;
+      row += ncl;
+      g_row = row < P.N ? __ldg(P.g + row) : 0.0f;
+      float m = -INFINITY;
+      if (len > 0) {
+        mbar_wait(&full[b], (uint32_t)(v / nb) & 1u, STT_DEVERR_CE_WAIT);
+#pragma unroll
+        for (int k = 0; k < kPVec; ++k) {
+          const int i = tid + k * kPConsumers;
+          if (i < n4) {
+            cur.e[k] = zs4[i];
+            cur.p[k] = ps4[i];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);  // this warp is done with buffer b
+#pragma unroll
+        for (int k = 0; k < kPVec; ++k) {
+          const int i = tid + k * kPConsumers;
+          if (i < n4)
+            m = fmaxf(m, fmaxf(fmaxf(cur.e[k].x, cur.e[k].y), fmaxf(cur.e[k].z, cur.e[k].w)));
+        }
+      }
+      m = warp_max(m);
+      cur.m = m;
+      float l = 0.f, sp = 0.f, spz = 0.f;
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int k = 0; k < kPVec; ++k) {
+          const int i = tid + k * kPConsumers;
+          if (i < n4) {
+            const float4 zv = cur.e[k];
+            const float4 pv = cur.p[k];
+            float4 e;
+            e.x = ex2(fmaf(zv.x, kLog2e, -mb));
+            e.y = ex2(fmaf(zv.y, kLog2e, -mb));
+            e.z = ex2(fmaf(zv.z, kLog2e, -mb));
+            e.w = ex2(fmaf(zv.w, kLog2e, -mb));
+            l += (e.x + e.y) + (e.z + e.w);
+            sp += (pv.x + pv.y) + (pv.z + pv.w);
+            spz = fmaf(pv.x, zv.x, spz);
+            spz = fmaf(pv.y, zv.y, spz);
+            spz = fmaf(pv.z, zv.z, spz);
+            spz = fmaf(pv.w, zv.w, spz);
+            cur.e[k] = e;
+          }
+        }
+      }
+      l = warp_sum(l);
+      sp = warp_sum(sp);
+      spz = warp_sum(spz);
+      if (tid == 0) mbar_arrive_expect_tx(&xbar[v & 3], 16u * (uint32_t)(C * kPWarps));
+      if (lane < C)
+        st_async_f4(mapa_shared(smem_u32(&stats[v & 3][rank * kPWarps + warp]), (uint32_t)lane),
+                    make_float4(m, l, sp, spz), mapa_shared(smem_u32(&xbar[v & 3]), (uint32_t)lane));
+    };
+
+    // finish(u) of the row kept in `prv`.
+    auto finish = [&](const CeRowRegs& prv, int u) {
+      mbar_wait_cluster(&xbar[u & 3], (uint32_t)(u >> 2) & 1u, STT_DEVERR_CE_WAIT);
+      const int np = C * kPWarps;
+      float4 q[kPParts / 32];
+      float M = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kPParts / 32; ++t) {
+        const int j = lane + 32 * t;
+        q[t] = j < np ? stats[u & 3][j] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        M = fmaxf(M, q[t].x);
+      }
+      M = warp_max(M);
+      float Ls = 0.f, Sp = 0.f, Spz = 0.f;
+#pragma unroll
+      for (int t = 0; t < kPParts / 32; ++t) {
+        if (q[t].y > 0.f) Ls += q[t].y * ex2((q[t].x - M) * kLog2e);
+        Sp += q[t].z;
+        Spz += q[t].w;
+      }
+      Ls = warp_sum(Ls);
+      Sp = warp_sum(Sp);
+      Spz = warp_sum(Spz);
+      const float lse = M + logf(Ls);
+      const float g = prv.g;
+      // exp(z - lse) g Sp = e exp(m_w - lse) g Sp; m_w <= lse, so this cannot overflow.
+      const float scale = (prv.m == -INFINITY) ? 0.f : ex2((prv.m - lse) * kLog2e) * (g * Sp);
+      float* zrow = P.z + prv.row * P.V + begin;
+#pragma unroll
+      for (int k = 0; k < kPVec; ++k) {
+        const int i = tid + k * kPConsumers;
+        if (i < n4) {
+          float4 o;
+          o.x = fmaf(prv.e[k].x, scale, -prv.p[k].x * g);
+          o.y = fmaf(prv.e[k].y, scale, -prv.p[k].y * g);
+          o.z = fmaf(prv.e[k].z, scale, -prv.p[k].z * g);
+          o.w = fmaf(prv.e[k].w, scale, -prv.p[k].w * g);
+          st_global_cs_f4(zrow + 4 * i, o);
+        }
+      }
+      if (rank == 0 && tid == 0) {
+        const float ell = fmaf(lse, Sp, -Spz);
+        if (P.row_loss) P.row_loss[prv.row] = ell;
+        P.wl[prv.row] = g * ell;
+      }
+    };
+
+    // Two register sets, alternating, so that each stays in registers.
+    while (true) {
+      if (!next_valid()) break;
+      reduce(ra);
+      if (v > 0) finish(rb, v - 1);
+      ++v;
+      if (!next_valid()) break;
+      reduce(rb);
+      finish(ra, v - 1);
+      ++v;
+    }
+    if (v > 0) {
+      if ((v - 1) & 1)
+        finish(rb, v - 1);
+      else
+        finish(ra, v - 1);
+    }
+  }
+  // Every CTA stays until the whole cluster is done, so no push can target a
+  // CTA that has left, even after a timed-out wait.
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+}
+
 // Fixed-order sum of the per-row weighted losses (one CTA, deterministic).
 __global__ void __launch_bounds__(1024) soft_ce_loss_sum(const float* wl, long long N,
                                                          float* loss) {
@@ -262,8 +551,10 @@ __global__ void __launch_bounds__(1024) soft_ce_loss_sum(const float* wl, long l
 
 }  // namespace
 
-CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
-  (void)N;
+namespace {
+
+// One cluster per row (the non-persistent kernel).
+CePlan soft_ce_plan_cta(const float* z, const float* p, int64_t V) {
   CePlan plan;
   plan.bulk = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0) &&
               ((reinterpret_cast<uintptr_t>(p) & 15u) == 0);
@@ -280,30 +571,134 @@ CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
   plan.C = (int)C;
   plan.slice = (int)slice;
   plan.smem = (int)(8 * slice);
+  plan.persistent = false;
+  plan.nb = 1;
   return plan;
 }
+
+}  // namespace
+
+CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
+  (void)N;
+  CePlan plan = soft_ce_plan_cta(z, p, V);
+  if (plan.bulk) {
+    // Persistent clusters: slices of about kPSliceTarget elements, at least
+    // kPMinBufs row buffers per CTA.
+    long long Cp = (V + kPSliceTarget - 1) / kPSliceTarget;
+    const long long Cmin = (V + kPSliceMax - 1) / kPSliceMax;
+    if (Cp < Cmin) Cp = Cmin;
+    if (Cp < 1) Cp = 1;
+    if (Cp > kMaxCluster) Cp = kMaxCluster;
+    long long sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
+    while (Cp > 1 && (Cp - 1) * sl >= V) {
+      --Cp;
+      sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
+    }
+    long long nb = kPSmemBudget / (8 * sl);
+    if (nb > kPMaxBufs) nb = kPMaxBufs;
+    if (sl <= kPSliceMax && nb >= kPMinBufs) {
+      plan.persistent = true;
+      plan.C = (int)Cp;
+      plan.slice = (int)sl;
+      plan.nb = (int)nb;
+      plan.smem = (int)(nb * 8 * sl);
+    }
+  }
+  return plan;
+}
+
+namespace {
+
+// Co-resident clusters of the persistent kernel for (C, smem) on the current
+// device; 0 if the query fails.  Cached per device for the last configuration.
+int persistent_clusters(int C, int smem) {
+  static std::mutex mu;
+  static int cache_dev[64], cache_C[64], cache_smem[64], cache_n[64];
+  static bool init = false;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (int i = 0; i < 64; ++i) cache_dev[i] = -1;
+    init = true;
+  }
+  if (cache_dev[dev] == dev && cache_C[dev] == C && cache_smem[dev] == smem) return cache_n[dev];
+  if (cudaFuncSetAttribute(soft_ce_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return 0;
+  if (C > 8 && cudaFuncSetAttribute(soft_ce_persistent_kernel,
+                                    cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                    1) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, soft_ce_persistent_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cache_dev[dev] = dev;
+  cache_C[dev] = C;
+  cache_smem[dev] = smem;
+  cache_n[dev] = n;
+  return n;
+}
+
+}  // namespace
 
 cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const float* g,
                            int64_t N, int64_t V, float* row_loss, float* loss, float* wl,
                            cudaStream_t s) {
-  if (N > 0) {
-    CeParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, plan.C, plan.slice};
-    void (*kern)(const CeParams) = plan.bulk ? soft_ce_kernel<true> : soft_ce_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         plan.smem);
-    if (e != cudaSuccess) return e;
-    if (plan.C > 8) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
+  const int ncl = (N > 0 && plan.persistent) ? persistent_clusters(plan.C, plan.smem) : 0;
+  if (ncl > 0) {
+    const long long n_clusters = ncl < N ? ncl : N;
+    CePParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, plan.C, plan.slice, plan.nb};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(N * plan.C), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.gridDim = dim3((unsigned)(n_clusters * plan.C), 1, 1);
+    cfg.blockDim = dim3(kPThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)plan.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)plan.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    prof_before(s, STT_KERNEL_SOFT_CE);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel, P);
+    prof_after(s);
+    if (e != cudaSuccess) return e;
+  } else if (N > 0) {
+    // One cluster per row (also taken if the persistent kernel cannot be resident).
+    const CePlan fb = plan.persistent ? soft_ce_plan_cta(z, p, V) : plan;
+    if (N * (long long)fb.C > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    CeParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, fb.C, fb.slice};
+    void (*kern)(const CeParams) = fb.bulk ? soft_ce_kernel<true> : soft_ce_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         fb.smem);
+    if (e != cudaSuccess) return e;
+    if (fb.C > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(N * fb.C), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)fb.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)fb.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -389,5 +784,6 @@ namespace stt {
 static_assert(kSliceMax * 8 <= 227 * 1024, "slice must fit in shared memory");
 static_assert((long long)kSliceMax * kMaxCluster == kCeMaxV, "max V");
 static_assert(kSliceMax <= kChunk * kMaxChunks, "chunks");
+static_assert(kPSmemBudget + 2048 <= 227 * 1024, "persistent shared memory");
 
 }  // namespace stt
