@@ -447,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = (issued_do > NS ? issued_do - NS : 0); i < issued_do; ++i)
           mbar_wait(&bar_do_full[i % NS], (uint32_t)(i / NS) & 1u, STT_DEVERR_BWD_WAIT);
       }
-      bulk_wait_group0();
+      // The reduce-adds complete with the grid; the CTA only has to stay
+      // until TMA has read their shared-memory sources.
+      bulk_wait_group_read0();
     }
   } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ------------------------------------------------------- MMA issuers --
@@ -746,9 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_reduce_add_3d(&tmDK, smem + (D / 32 + cc) * L::kStageBlkB, cc * 32, c0, bhk);
         }
         bulk_commit_group();
-        // The issuing thread waits for its reductions before the CTA's shared
-        // memory goes away.
-        bulk_wait_group0();
+        // The issuing thread waits until TMA has read the staging before the
+        // CTA's shared memory goes away; the reductions complete with the grid.
+        bulk_wait_group_read0();
       }
     }
   }

@@ -100,7 +100,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ FwdParams P, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ SfxMaps sfx) {
+                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ SfxMaps sfx) {
   using L = FwdSmem<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -452,18 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run += s_sum[half ^ 1][r];
     }
     if (ok) {
+      // O (bf16) is staged in the Q buffer, which every reader is done with
+      // (the last S product and, behind the group barrier above, the suffix
+      // dot products), in the swizzled layout of the tile loads, and leaves
+      // through one TMA store; rows past Q_LEN are clipped by TMA.
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      if (qrow < P.Q_LEN) {
-        uint4* op = reinterpret_cast<uint4*>(P.out + ((size_t)bh * P.Q_LEN + qrow) * D + half * DH);
 #pragma unroll
-        for (int c = 0; c < DH / 8; ++c)
-          op[c] = make_uint4(pack_bf16(o[c * 8 + 0] * inv_l, o[c * 8 + 1] * inv_l),
-                             pack_bf16(o[c * 8 + 2] * inv_l, o[c * 8 + 3] * inv_l),
-                             pack_bf16(o[c * 8 + 4] * inv_l, o[c * 8 + 5] * inv_l),
-                             pack_bf16(o[c * 8 + 6] * inv_l, o[c * 8 + 7] * inv_l));
-        if (half == 0)
-          P.lse[(size_t)bh * P.Q_LEN + qrow] =
-              l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      for (int c = 0; c < DH / 8; ++c)
+        *reinterpret_cast<uint4*>(sQ + swz_chunk_offset(r, half * (DH / 8) + c, kTile)) =
+            make_uint4(pack_bf16(o[c * 8 + 0] * inv_l, o[c * 8 + 1] * inv_l),
+                       pack_bf16(o[c * 8 + 2] * inv_l, o[c * 8 + 3] * inv_l),
+                       pack_bf16(o[c * 8 + 4] * inv_l, o[c * 8 + 5] * inv_l),
+                       pack_bf16(o[c * 8 + 6] * inv_l, o[c * 8 + 7] * inv_l));
+      if (half == 0 && qrow < P.Q_LEN)
+        P.lse[(size_t)bh * P.Q_LEN + qrow] =
+            l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
+      if (ok && tid == 0) {
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_store_3d(&tmO, sQ + cb * kTile * 128, cb * kColBlock, q0, bh);
+        bulk_commit_group();
       }
     }
   }
@@ -474,14 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // The O store completes with the grid; its source must be read first.
+  if (tid == 0) bulk_wait_group_read0();
 }
 
 template <int D>
 cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
-  CUtensorMap tmQ, tmK, tmV;
+  CUtensorMap tmQ, tmK, tmV, tmO;
   static thread_local SfxMaps sfx;
   cudaError_t e;
   if ((e = encode_tile_map(&tmQ, a.q, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
+  if ((e = encode_tile_map(&tmO, out, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmK, a.k_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
   if ((e = encode_tile_map(&tmV, a.v_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
@@ -511,7 +523,7 @@ cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(P.n_qt * a.H * a.B);
   prof_before(s, STT_KERNEL_ATTN_FWD);
-  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(P, tmQ, tmK, tmV, sfx);
+  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(P, tmQ, tmK, tmV, tmO, sfx);
   prof_after(s);
   return cudaGetLastError();
 }

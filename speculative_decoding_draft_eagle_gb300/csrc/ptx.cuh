@@ -177,6 +177,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* map, const void* s
       "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 3-D tiled store shared -> global, tracked by the issuing thread's bulk
+// groups.  Rows past the tensor's extent are clipped.
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -188,10 +198,6 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 // shared memory.
 __device__ __forceinline__ void bulk_wait_group_read1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-// Wait until this thread's bulk groups have fully completed.
-__device__ __forceinline__ void bulk_wait_group0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Untiled bulk copy global -> shared (16-byte aligned addresses, bytes % 16 == 0).
