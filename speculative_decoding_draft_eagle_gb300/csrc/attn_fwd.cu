@@ -75,12 +75,14 @@ constexpr int kSBufs = 3;
 constexpr uint32_t kColS0 = 0, kColO = kSBufs * kTile;
 static_assert(kColO + 128 <= kTmemCols, "three S buffers and O fit in TMEM");
 
-// Dot product of row r of two swizzled [128 x D] bf16 tiles in shared memory.
+// Dot product of half h of row r of two swizzled [128 x D] bf16 tiles in
+// shared memory.
 template <int D>
-__device__ __forceinline__ float smem_row_dot(const unsigned char* a, const unsigned char* b, int r) {
+__device__ __forceinline__ float smem_half_row_dot(const unsigned char* a, const unsigned char* b,
+                                                   int r, int h) {
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c) {
+  for (int c = h * (D / 16); c < (h + 1) * (D / 16); ++c) {
     const uint32_t off = swz_chunk_offset(r, c, kTile);
     const uint4 x = *reinterpret_cast<const uint4*>(a + off);
     const uint4 y = *reinterpret_cast<const uint4*>(b + off);
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
   __shared__ float s_sum[2][kTile];     // [half][row] partial row sum
+  __shared__ float s_dot[2][2][kTile];  // [block parity][half][row] partial suffix score
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -185,22 +188,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued_s = 0;
       bool ok = issued_v == n_kv;
-      // Suffix tiles reuse the K/V stage buffers once every MMA has finished.
-      if (ok && n_sfx > 0) ok = mbar_wait(&bar_drain, 0, STT_DEVERR_FWD_WAIT);
-      for (int j = 1; ok && j <= n_sfx; ++j) {
-        const int st = (j - 1) % kStages;
-        const uint32_t ph = (uint32_t)((j - 1) / kStages) & 1u;
-        if (j > kStages && !mbar_wait(&bar_sfx_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) {
+      // Suffix tiles continue the K/V stage sequence: suffix block w + 1 takes
+      // stage (n_kv + w) % kStages.  Its K half is loaded as soon as the S
+      // product of the stage's last causal tile has read the K buffer, its V
+      // half once the P V product has read the V buffer; a stage's later
+      // suffix uses wait for the softmax warps to release it.
+      for (int w = 0; ok && w < n_sfx; ++w) {
+        const int u = n_kv + w;
+        const int st = u % kStages;
+        const int m = w / kStages;  // earlier suffix uses of this stage
+        if (m == 0) {
+          if (u >= kStages &&
+              !mbar_wait(&bar_k_empty[st], (uint32_t)(u / kStages - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
+            ok = false;
+            break;
+          }
+        } else if (!mbar_wait(&bar_sfx_empty[st], (uint32_t)(m - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(&bar_sfx_full[st], 2 * L::kKV);
-        for (int cb = 0; cb < D / kColBlock; ++cb) {
-          tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &sfx.k[j - 1],
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &sfx.k[w],
                       &bar_sfx_full[st], cb * kColBlock, q0, bhk);
-          tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &sfx.v[j - 1],
-                      &bar_sfx_full[st], cb * kColBlock, q0, bhk);
+        if (m == 0 && u >= kStages &&
+            !mbar_wait(&bar_v_empty[st], (uint32_t)(u / kStages - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
+          ok = false;
+          ++issued_s;
+          break;
         }
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &sfx.v[w],
+                      &bar_sfx_full[st], cb * kColBlock, q0, bhk);
         ++issued_s;
       }
       if (issued_v < n_kv) {
@@ -213,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok)
         for (int i = (issued_s > kStages ? issued_s - kStages : 0); i < issued_s; ++i)
-          mbar_wait(&bar_sfx_full[i % kStages], (uint32_t)(i / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+          mbar_wait(&bar_sfx_full[(n_kv + i) % kStages], (uint32_t)(i / kStages) & 1u,
+                    STT_DEVERR_FWD_WAIT);
     }
   } else if (warp == kWarpMma || warp == kWarpPv) {
     // ------------------------------------------------------- MMA issuers --
@@ -411,15 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------- suffix keys (blocks 1..k) --
     // Query q < T sees key q of every later block: one score per block, a
     // register-level online-softmax update of this thread's O half.
+    // The two threads of a row each take half of the score's dot product and
+    // exchange the halves through shared memory.
     const bool sfx_row = qrow < T;
-    for (int j = 1; ok && j <= n_sfx; ++j) {
-      const int st = (j - 1) % kStages;
-      ok = warp_wait(&bar_sfx_full[st], (uint32_t)((j - 1) / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+    for (int w = 0; ok && w < n_sfx; ++w) {
+      const int st = (n_kv + w) % kStages;
+      ok = warp_wait(&bar_sfx_full[st], (uint32_t)(w / kStages) & 1u, STT_DEVERR_FWD_WAIT);
+      if (!ok) break;
+      const unsigned char* sK = smem + L::k0 + st * L::kKV;
+      const unsigned char* sV = smem + L::v0 + st * L::kKV;
+      s_dot[w & 1][half][r] = sfx_row ? smem_half_row_dot<D>(sQ, sK, r, half) : 0.f;
+      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       if (sfx_row) {
-        const unsigned char* sK = smem + L::k0 + st * L::kKV;
-        const unsigned char* sV = smem + L::v0 + st * L::kKV;
-        const float sj = smem_row_dot<D>(sQ, sK, r) * sl2;
+        const float sj = (s_dot[w & 1][0][r] + s_dot[w & 1][1][r]) * sl2;
         if (sj > m_run) {
           const float alpha = ex2(m_run - sj);  // 0 when m_run is -inf
           l_run *= alpha;
