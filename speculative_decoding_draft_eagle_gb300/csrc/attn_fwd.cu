@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
 
       const int cbase = j * kTile + half * 64;
-      float mt = -INFINITY;
+      // Eight independent partial maxima (a tree instead of one 64-long chain).
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
       if (cbase + 63 <= lim) {
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2)
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float x = __uint_as_float(s[c2][i]) * sl2;
             s[c2][i] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
+            mp[i & 7] = fmaxf(mp[i & 7], x);
           }
       } else {
 #pragma unroll
@@ -329,9 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float x = (cbase + c2 * 32 + i <= lim) ? __uint_as_float(s[c2][i]) * sl2 : -INFINITY;
             s[c2][i] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
+            mp[i & 7] = fmaxf(mp[i & 7], x);
           }
       }
+      float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       // Combine the two halves' maxima (buffer double-buffered by tile parity).
       s_max[j & 1][half][r] = mt;
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
@@ -349,17 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       uint32_t pk[32];
-      float rs = 0.f;
+      float rp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) rp[k] = 0.f;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float p0 = ex2(__uint_as_float(s[c2][i]) - m_use);
           const float p1 = ex2(__uint_as_float(s[c2][i + 1]) - m_use);
-          rs += p0 + p1;
+          rp[(i >> 1) & 7] += p0 + p1;
           pk[(c2 * 32 + i) >> 1] = pack_bf16(p0, p1);
         }
-      l_run += rs;
+      l_run += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
 
       // P(j) goes to its own S buffer, and O += P(j) V(j) is ordered after
       // O += P(j-1) V(j-1) on the tensor pipe, so only a rescale of O has to
