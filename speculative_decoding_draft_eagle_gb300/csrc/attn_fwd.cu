@@ -23,8 +23,9 @@
 //              over their own S columns in TMEM, rescale O in TMEM when the
 //              running max grows by more than 2^8, and finish with the suffix
 //              keys and O / lse.
-//   warp 8     TMA producer (one lane): Q once, then K/V tiles (2 stages),
-//              then the suffix K_j / V_j tiles through the same buffers.
+//   warp 8     TMA producer (two lanes: Q and K, V): Q once, then K/V tiles
+//              (2 stages), then the suffix K_j / V_j tiles through the same
+//              buffers.
 //   warp 9     S issuer (one lane): S(j) into TMEM buffer j % 3 as soon as
 //              K(j) is in and O += P(j-3) V has read the buffer.
 //   warp 10    P V issuer (one lane): O += P(j) V(j), P read from TMEM.  Two
@@ -107,11 +108,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // s_full / s_free per S buffer (S(j) uses buffer j % 3); p_full alternates
-  // by tile parity so that a waiter can never miss a phase; o_done counts
-  // every O += P V.
+  // s_full / s_free per S buffer (S(j) uses buffer j % 3); p_full and o_done
+  // alternate by tile parity so that a waiter can never miss a phase: when the
+  // softmax warps hold S(j), O += P(j-3) V is complete (S(j) reused its
+  // buffer), so O += P(j-2) V and O += P(j-1) V may both still be pending, and
+  // one barrier counting every product could then not tell them apart.
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
-      bar_v_empty[kStages], bar_s_full[kSBufs], bar_s_free[kSBufs], bar_p_full[2], bar_o_done,
+      bar_v_empty[kStages], bar_s_full[kSBufs], bar_s_free[kSBufs], bar_p_full[2], bar_o_done[2],
       bar_drain, bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_v_full[s], 1);
       mbar_init(&bar_k_empty[s], 1);
       mbar_init(&bar_v_empty[s], 1);
-      mbar_init(&bar_sfx_full[s], 1);
+      mbar_init(&bar_sfx_full[s], 2);  // one arrival per producer lane
       mbar_init(&bar_sfx_empty[s], kSoftmaxWarps);
     }
     for (int s = 0; s < kSBufs; ++s) {
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_s_free[s], 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(&bar_p_full[s], kSoftmaxWarps);
-    mbar_init(&bar_o_done, 1);
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_o_done[s], 1);
     mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kSoftmaxWarps);
     fence_mbar_init();
@@ -161,45 +164,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0 && n_kv > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // Lane 0 loads Q and the K tiles, lane 1 the V tiles, so that a K load
+    // never queues behind a V stage that O += P V still holds.
+    if (lane < 2 && n_kv > 0) {
+      const bool is_k = lane == 0;
       const int bhk = b * P.H_kv + hk;
-      mbar_arrive_expect_tx(&bar_q, L::kQ);
-      for (int cb = 0; cb < D / kColBlock; ++cb)
-        tma_load_3d(sQ + cb * kTile * 128, &tmQ, &bar_q, cb * kColBlock, q0, bh);
-      int issued_k = 0, issued_v = 0;
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        mbar_arrive_expect_tx(&bar_q, L::kQ);
+        for (int cb = 0; cb < D / kColBlock; ++cb)
+          tma_load_3d(sQ + cb * kTile * 128, &tmQ, &bar_q, cb * kColBlock, q0, bh);
+      } else {
+        tma_prefetch_desc(&tmV);
+      }
+      unsigned char* const base = smem + (is_k ? L::k0 : L::v0);
+      const CUtensorMap* const tm = is_k ? &tmK : &tmV;
+      uint64_t* const full = is_k ? bar_k_full : bar_v_full;
+      uint64_t* const empty = is_k ? bar_k_empty : bar_v_empty;
+      bool ok = true;
+      int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kStages;
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-        if (j >= kStages && !mbar_wait(&bar_k_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) break;
-        mbar_arrive_expect_tx(&bar_k_full[st], L::kKV);
+        if (j >= kStages && !mbar_wait(&empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], L::kKV);
         for (int cb = 0; cb < D / kColBlock; ++cb)
-          tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &tmK, &bar_k_full[st],
-                      cb * kColBlock, j * kTile, bhk);
-        ++issued_k;
-        if (j >= kStages && !mbar_wait(&bar_v_empty[st], ph ^ 1u, STT_DEVERR_FWD_WAIT)) break;
-        mbar_arrive_expect_tx(&bar_v_full[st], L::kKV);
-        for (int cb = 0; cb < D / kColBlock; ++cb)
-          tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &tmV, &bar_v_full[st],
-                      cb * kColBlock, j * kTile, bhk);
-        ++issued_v;
+          tma_load_3d(base + st * L::kKV + cb * kTile * 128, tm, &full[st], cb * kColBlock,
+                      j * kTile, bhk);
+        ++issued;
       }
-      int issued_s = 0;
-      bool ok = issued_v == n_kv;
       // Suffix tiles continue the K/V stage sequence: suffix block w + 1 takes
       // stage (n_kv + w) % kStages.  Its K half is loaded as soon as the S
       // product of the stage's last causal tile has read the K buffer, its V
       // half once the P V product has read the V buffer; a stage's later
-      // suffix uses wait for the softmax warps to release it.
+      // suffix uses wait for the softmax warps to release it.  The suffix
+      // barrier counts one arrival from each lane.
+      int issued_s = 0;
       for (int w = 0; ok && w < n_sfx; ++w) {
         const int u = n_kv + w;
         const int st = u % kStages;
         const int m = w / kStages;  // earlier suffix uses of this stage
         if (m == 0) {
           if (u >= kStages &&
-              !mbar_wait(&bar_k_empty[st], (uint32_t)(u / kStages - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
+              !mbar_wait(&empty[st], (uint32_t)(u / kStages - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
             ok = false;
             break;
           }
@@ -207,33 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bar_sfx_full[st], 2 * L::kKV);
+        mbar_arrive_expect_tx(&bar_sfx_full[st], L::kKV);
         for (int cb = 0; cb < D / kColBlock; ++cb)
-          tma_load_3d(smem + L::k0 + st * L::kKV + cb * kTile * 128, &sfx.k[w],
-                      &bar_sfx_full[st], cb * kColBlock, q0, bhk);
-        if (m == 0 && u >= kStages &&
-            !mbar_wait(&bar_v_empty[st], (uint32_t)(u / kStages - 1) & 1u, STT_DEVERR_FWD_WAIT)) {
-          ok = false;
-          ++issued_s;
-          break;
-        }
-        for (int cb = 0; cb < D / kColBlock; ++cb)
-          tma_load_3d(smem + L::v0 + st * L::kKV + cb * kTile * 128, &sfx.v[w],
+          tma_load_3d(base + st * L::kKV + cb * kTile * 128, is_k ? &sfx.k[w] : &sfx.v[w],
                       &bar_sfx_full[st], cb * kColBlock, q0, bhk);
         ++issued_s;
       }
-      if (issued_v < n_kv) {
-        // Gave up: let every copy already issued land before the CTA exits.
-        mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
-        for (int j = (issued_k > kStages ? issued_k - kStages : 0); j < issued_k; ++j)
-          mbar_wait(&bar_k_full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
-        for (int j = (issued_v > kStages ? issued_v - kStages : 0); j < issued_v; ++j)
-          mbar_wait(&bar_v_full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
-      }
-      if (!ok)
+      if (!ok) {
+        // Gave up: let every copy this lane issued land before the CTA exits.
+        if (is_k) mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
+        for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+          mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
         for (int i = (issued_s > kStages ? issued_s - kStages : 0); i < issued_s; ++i)
           mbar_wait(&bar_sfx_full[(n_kv + i) % kStages], (uint32_t)(i / kStages) & 1u,
                     STT_DEVERR_FWD_WAIT);
+      }
     }
   } else if (warp == kWarpMma || warp == kWarpPv) {
     // ------------------------------------------------------- MMA issuers --
@@ -280,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(dV, kk * 2048),
                          idO, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_o_done);
+          umma_commit(&bar_o_done[i & 1]);
           umma_commit(&bar_s_free[sb]);
           umma_commit(&bar_v_empty[st]);
         }
@@ -370,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // P(j) goes to its own S buffer, and O += P(j) V(j) is ordered after
       // O += P(j-1) V(j-1) on the tensor pipe, so only a rescale of O has to
-      // wait for the previous product (its phase is the newest one possible:
-      // the next needs this tile's P).
+      // wait for the previous product (its commit also covers every earlier
+      // one of the issuing thread).
       if (__any_sync(0xffffffffu, rescale_o)) {
-        ok = warp_wait(&bar_o_done, (uint32_t)(j - 1) & 1u, STT_DEVERR_FWD_WAIT);
+        ok = warp_wait(&bar_o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, STT_DEVERR_FWD_WAIT);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -405,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bar_p_full[j & 1]);
     }
     if (ok && n_kv > 0) {
-      ok = warp_wait(&bar_o_done, (uint32_t)(n_kv - 1) & 1u, STT_DEVERR_FWD_WAIT);
+      // Every product is complete (the issuers' drain barrier fires once).
+      ok = warp_wait(&bar_drain, 0, STT_DEVERR_FWD_WAIT);
       tc_fence_after();
     }
 
