@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_dp_full, bar_p_ready, bar_pt_free, bar_ds_ready, bar_dq_full, bar_dk_done, bar_dq_free,
       bar_stg_full, bar_stg_done, bar_final, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
-  // [tile parity][lse2 | Delta][query]: tile i's statistics sit in buffer i & 1.
+  // [tile parity][-lse2 | -Delta][query]: tile i's statistics sit in buffer i & 1.
   __shared__ __align__(16) float s_stat[2][2][kTile];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -604,9 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = P.scale_log2;
     const bool kv_live = kv < T;  // T <= Q_LEN, so also kv < Q_LEN
     unsigned char* sDS = smem + L::ds;
-    // Thread tid stages one statistic of one query of a tile: lse2 (tid < 128)
-    // or Delta (tid >= 128) of query tq0 + (tid & 127).  The raw value is
-    // fetched a tile ahead and scaled only when it is stored.
+    // Thread tid stages one statistic of one query of a tile: -lse2 (tid < 128)
+    // or -Delta (tid >= 128) of query tq0 + (tid & 127), negated for the
+    // packed FMA / add below.  The raw value is fetched a tile ahead and
+    // scaled only when it is stored.
     const int st_which = tid >> 7, st_idx = tid & 127;
     auto fetch_stat = [&](int i) -> float {
       const int qq = (t_first + i) * kTile + st_idx;
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return st_which == 0 ? P.lse[rq] : P.delta[rq];
     };
     auto put_stat = [&](int buf, float raw) {
-      s_stat[buf][st_which][st_idx] = st_which == 0 ? raw * kLog2e : raw;
+      s_stat[buf][st_which][st_idx] = st_which == 0 ? -raw * kLog2e : -raw;
     };
     uint32_t grp_uses = 0;
     bool ok = true;
@@ -632,8 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qh = tq0 + half * 64;  // first query of this thread's half
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
       const bool full = kv_live && kv <= qh && qh + 64 <= P.Q_LEN;
-      const float* lse_s = s_stat[par][0] + half * 64;
-      const float* dl_s = s_stat[par][1] + half * 64;
+      const float* nlse_s = s_stat[par][0] + half * 64;
+      const float* ndl_s = s_stat[par][1] + half * 64;
 
       // ---- P^T = exp(S^T - lse): queries [qh, qh + 64) of key row kv.  The
       // fp32 P overwrites the loaded S^T values (it is needed again for dS).
@@ -643,16 +644,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pf[2][32];
       tmem_ld32x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColS + half * 64 + 32,
                   pf[0], pf[1]);
+      const uint64_t sl2x2 = f32x2(sl2, sl2);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pp[16];
 #pragma unroll
         for (int x4 = 0; x4 < 32; x4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c2 * 32 + x4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          // 2^(S sl2 - lse2), two queries per packed FMA
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + c2 * 32 + x4);
+          float xv[4];
+          unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1])),
+                                 sl2x2, f32x2(l4.x, l4.y)),
+                       xv[0], xv[1]);
+          unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3])),
+                                 sl2x2, f32x2(l4.z, l4.w)),
+                       xv[2], xv[3]);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float pv = ex2(fmaf(__uint_as_float(pf[c2][x4 + e]), sl2, -lv[e]));
+            float pv = ex2(xv[e]);
             if (!full) {
               const int qa = qh + c2 * 32 + x4 + e;
               if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv = 0.f;
@@ -683,12 +692,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_off + kColDP + half * 64 + c2 * 32, dp);
 #pragma unroll
         for (int x4 = 0; x4 < 32; x4 += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dl_s + c2 * 32 + x4);
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          // P (dP - Delta), two queries per packed add and multiply
+          const float4 d4 = *reinterpret_cast<const float4*>(ndl_s + c2 * 32 + x4);
           float sv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            sv[e] = __uint_as_float(pf[c2][x4 + e]) * (__uint_as_float(dp[x4 + e]) - dv[e]);
+          unpack_f32x2(mul_f32x2(f32x2(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1])),
+                                 add_f32x2(f32x2(__uint_as_float(dp[x4]), __uint_as_float(dp[x4 + 1])),
+                                           f32x2(d4.x, d4.y))),
+                       sv[0], sv[1]);
+          unpack_f32x2(mul_f32x2(f32x2(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3])),
+                                 add_f32x2(f32x2(__uint_as_float(dp[x4 + 2]), __uint_as_float(dp[x4 + 3])),
+                                           f32x2(d4.z, d4.w))),
+                       sv[2], sv[3]);
           dd[x4 >> 1] = pack_bf16(sv[0], sv[1]);
           dd[(x4 >> 1) + 1] = pack_bf16(sv[2], sv[3]);
         }

@@ -18,7 +18,8 @@
 // Warp roles (352 threads, one CTA per 128-row query tile of one head):
 //   warps 0-7  softmax: warps w and w+4 own the 32 query rows of TMEM lane
 //              quarter w%4 and split the 128 key columns (and O's D columns)
-//              in halves; the row max is exchanged through shared memory.
+//              in halves; the row max is exchanged through shared memory
+//              between the two warps of a quarter.
 //              They load S from TMEM, mask, exponentiate, write P (bf16) back
 //              over their own S columns in TMEM, rescale O in TMEM when the
 //              running max grows by more than 2^8, and finish with the suffix
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // one barrier counting every product could then not tell them apart.
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
       bar_v_empty[kStages], bar_s_full[kSBufs], bar_s_free[kSBufs], bar_p_full[2], bar_o_done[2],
-      bar_drain, bar_grp, bar_sfx_full[kStages], bar_sfx_empty[kStages];
+      bar_drain, bar_grp, bar_pair[4], bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
   __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
   __shared__ float s_sum[2][kTile];     // [half][row] partial row sum
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) mbar_init(&bar_o_done[s], 1);
     mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kSoftmaxWarps);
+    for (int q = 0; q < 4; ++q) mbar_init(&bar_pair[q], 2);  // warps q and q + 4
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = causal_row_limit(qrow, T);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = P.scale_log2;
-    uint32_t grp_uses = 0;
+    uint32_t grp_uses = 0, pair_uses = 0;
 
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -311,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
 
       const int cbase = j * kTile + half * 64;
-      // Eight independent partial maxima (a tree instead of one 64-long chain).
+      // Maximum of the raw scores (the scale is > 0 and is applied to the
+      // maximum alone), as eight independent three-input partial maxima.
       float mp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
@@ -319,26 +322,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(s[c2][i]) * sl2;
-            s[c2][i] = __float_as_uint(x);
-            mp[i & 7] = fmaxf(mp[i & 7], x);
-          }
+          for (int i = 0; i < 32; i += 2)
+            mp[(i >> 1) & 7] = fmax3(mp[(i >> 1) & 7], __uint_as_float(s[c2][i]),
+                                     __uint_as_float(s[c2][i + 1]));
       } else {
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float x = (cbase + c2 * 32 + i <= lim) ? __uint_as_float(s[c2][i]) * sl2 : -INFINITY;
+            const float x = (cbase + c2 * 32 + i <= lim) ? __uint_as_float(s[c2][i]) : -INFINITY;
             s[c2][i] = __float_as_uint(x);
             mp[i & 7] = fmaxf(mp[i & 7], x);
           }
       }
       float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
       // Combine the two halves' maxima (buffer double-buffered by tile parity).
+      // Only the two warps of a lane quarter meet here.
       s_max[j & 1][half][r] = mt;
-      ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
+      ok = group_sync(&bar_pair[quarter], pair_uses, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       mt = fmaxf(mt, s_max[j & 1][half ^ 1][r]);
 
@@ -352,20 +354,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale_o = j > 0;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // p = 2^(s sl2 - m): two elements per packed fp32x2 FMA, and the row sum
+      // in four packed partial accumulators.
       uint32_t pk[32];
-      float rp[8];
+      const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
+      uint64_t rp[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) rp[k] = 0.f;
+      for (int k = 0; k < 4; ++k) rp[k] = f32x2(0.f, 0.f);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2(__uint_as_float(s[c2][i]) - m_use);
-          const float p1 = ex2(__uint_as_float(s[c2][i + 1]) - m_use);
-          rp[(i >> 1) & 7] += p0 + p1;
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(s[c2][i]), __uint_as_float(s[c2][i + 1])),
+                                 sl2x2, negm2),
+                       x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          rp[(i >> 1) & 3] = add_f32x2(rp[(i >> 1) & 3], f32x2(p0, p1));
           pk[(c2 * 32 + i) >> 1] = pack_bf16(p0, p1);
         }
-      l_run += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+      float ra, rb;
+      unpack_f32x2(add_f32x2(add_f32x2(rp[0], rp[1]), add_f32x2(rp[2], rp[3])), ra, rb);
+      l_run += ra + rb;
 
       // P(j) goes to its own S buffer, and O += P(j) V(j) is ordered after
       // O += P(j-1) V(j-1) on the tensor pipe, so only a rescale of O has to
