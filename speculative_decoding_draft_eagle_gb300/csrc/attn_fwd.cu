@@ -18,8 +18,8 @@
 // Warp roles (352 threads, one CTA per 128-row query tile of one head):
 //   warps 0-7  softmax: warps w and w+4 own the 32 query rows of TMEM lane
 //              quarter w%4 and split the 128 key columns (and O's D columns)
-//              in halves; the row max is exchanged through shared memory
-//              between the two warps of a quarter.
+//              in halves ("parts"); the row max is exchanged through shared
+//              memory between the two warps of a quarter.
 //              They load S from TMEM, mask, exponentiate, write P (bf16) back
 //              over their own S columns in TMEM, rescale O in TMEM when the
 //              running max grows by more than 2^8, and finish with the suffix
@@ -39,10 +39,17 @@ namespace stt {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 352;
+// Two softmax warps per TMEM lane quarter (each a 64-key half of the tile).
+// Four per quarter (the code takes any of the two) measured slower, 882 vs
+// 927 TFLOP/s: the four-way max exchange and the extra arrivals cost more than
+// the added overlap gains.
 constexpr int kSoftmax = 256;
 constexpr int kSoftmaxWarps = kSoftmax / 32;  // barriers count one arrival per warp
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpPv = 10;
+constexpr int kParts = kSoftmaxWarps / 4;     // softmax warps per TMEM lane quarter
+constexpr int kPartCols = kTile / kParts;     // key columns per softmax thread and tile
+constexpr int kThreads = kSoftmax + 96;
+constexpr int kWarpTma = kSoftmaxWarps, kWarpMma = kSoftmaxWarps + 1, kWarpPv = kSoftmaxWarps + 2;
+static_assert(kPartCols == 32 || kPartCols == 64, "one or two 32-column TMEM loads per tile");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 between rescales
 
 struct FwdParams {
@@ -70,21 +77,22 @@ struct FwdSmem {
   static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
 };
 
-// TMEM columns: S buffers at 0, 128 and 256 (P of column half h is written
-// back into columns [64h, 64h + 32) of its S buffer), O at 384.
+// TMEM columns: S buffers at 0, 128 and 256 (P of softmax part p is written
+// back into columns [p kPartCols, + kPartCols / 2) of its S buffer, inside the
+// S columns that part itself reads), O at 384.
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;
 constexpr uint32_t kColS0 = 0, kColO = kSBufs * kTile;
 static_assert(kColO + 128 <= kTmemCols, "three S buffers and O fit in TMEM");
 
-// Dot product of half h of row r of two swizzled [128 x D] bf16 tiles in
-// shared memory.
-template <int D>
-__device__ __forceinline__ float smem_half_row_dot(const unsigned char* a, const unsigned char* b,
-                                                   int r, int h) {
+// Dot product of part p (of NP equal parts) of row r of two swizzled
+// [128 x D] bf16 tiles in shared memory.
+template <int D, int NP>
+__device__ __forceinline__ float smem_part_row_dot(const unsigned char* a, const unsigned char* b,
+                                                   int r, int p) {
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-  for (int c = h * (D / 16); c < (h + 1) * (D / 16); ++c) {
+  for (int c = p * (D / 8 / NP); c < (p + 1) * (D / 8 / NP); ++c) {
     const uint32_t off = swz_chunk_offset(r, c, kTile);
     const uint4 x = *reinterpret_cast<const uint4*>(a + off);
     const uint4 y = *reinterpret_cast<const uint4*>(b + off);
@@ -116,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // one barrier counting every product could then not tell them apart.
   __shared__ uint64_t bar_q, bar_k_full[kStages], bar_v_full[kStages], bar_k_empty[kStages],
       bar_v_empty[kStages], bar_s_full[kSBufs], bar_s_free[kSBufs], bar_p_full[2], bar_o_done[2],
-      bar_drain, bar_grp, bar_pair[4], bar_sfx_full[kStages], bar_sfx_empty[kStages];
+      bar_drain, bar_grp, bar_quad[4], bar_sfx_full[kStages], bar_sfx_empty[kStages];
   __shared__ uint32_t tmem_base;
-  __shared__ float s_max[2][2][kTile];  // [tile parity][half][row] partial row max
-  __shared__ float s_sum[2][kTile];     // [half][row] partial row sum
-  __shared__ float s_dot[2][2][kTile];  // [block parity][half][row] partial suffix score
+  __shared__ float s_max[2][kParts][kTile];  // [tile parity][part][row] partial row max
+  __shared__ float s_sum[kParts][kTile];     // [part][row] partial row sum
+  __shared__ float s_dot[2][kParts][kTile];  // [block parity][part][row] partial suffix score
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = P.H * P.B;
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) mbar_init(&bar_o_done[s], 1);
     mbar_init(&bar_drain, 2);  // one commit from each issuing thread
     mbar_init(&bar_grp, kSoftmaxWarps);
-    for (int q = 0; q < 4; ++q) mbar_init(&bar_pair[q], 2);  // warps q and q + 4
+    for (int q = 0; q < 4; ++q) mbar_init(&bar_quad[q], kParts);  // warps q, q + 4, ...
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -267,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bar_k_empty[st]);
         }
       } else {
-        // O += P(i) V(i): A = P in TMEM (keys 64h.. of the tile live at column
-        // 64h of its S buffer), B = V MN-major.
+        // O += P(i) V(i): A = P in TMEM (the keys of softmax part p live at
+        // column p kPartCols of its S buffer, 8 columns per 16 keys), B = V
+        // MN-major.
         for (int i = 0; ok && i < n_kv; ++i) {
           const int st = i % kStages, sb = i % kSBufs;
           ok = mbar_wait(&bar_p_full[i & 1], (uint32_t)(i >> 1) & 1u, STT_DEVERR_FWD_WAIT) &&
@@ -279,7 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t aP = tmem + kColS0 + sb * kTile;
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_ts(tmem + kColO, aP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(dV, kk * 2048),
+            umma_bf16_ts(tmem + kColO,
+                         aP + (kk / (kPartCols / 16)) * kPartCols + (kk % (kPartCols / 16)) * 8,
+                         sdesc_add(dV, kk * 2048),
                          idO, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bar_o_done[i & 1]);
           umma_commit(&bar_s_free[sb]);
@@ -293,13 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax --
-    const int quarter = warp & 3, half = warp >> 2;
+    constexpr int DH = D / kParts;  // O columns per thread
+    const int quarter = warp & 3, part = warp >> 2;
     const int r = quarter * 32 + lane;  // query row in the tile = TMEM lane
     const int qrow = q0 + r;
     const int lim = causal_row_limit(qrow, T);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = P.scale_log2;
-    uint32_t grp_uses = 0, pair_uses = 0;
+    uint32_t grp_uses = 0, quad_uses = 0;
+    constexpr int NC = kPartCols / 32;  // 32-column TMEM loads per tile
 
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -308,26 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&bar_s_full[sb], (uint32_t)(j / kSBufs) & 1u, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[2][32];
-      tmem_ld32x2(tmem + lane_off + kColS0 + sb * kTile + half * 64,
-                  tmem + lane_off + kColS0 + sb * kTile + half * 64 + 32, s[0], s[1]);
+      const uint32_t scol = tmem + lane_off + kColS0 + sb * kTile + part * kPartCols;
+      uint32_t s[NC][32];
+      if constexpr (NC == 2)
+        tmem_ld32x2(scol, scol + 32, s[0], s[1]);
+      else
+        tmem_ld32(scol, s[0]);
 
-      const int cbase = j * kTile + half * 64;
+      const int cbase = j * kTile + part * kPartCols;
       // Maximum of the raw scores (the scale is > 0 and is applied to the
       // maximum alone), as eight independent three-input partial maxima.
       float mp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
-      if (cbase + 63 <= lim) {
+      if (cbase + kPartCols - 1 <= lim) {
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2)
+        for (int c2 = 0; c2 < NC; ++c2)
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
             mp[(i >> 1) & 7] = fmax3(mp[(i >> 1) & 7], __uint_as_float(s[c2][i]),
                                      __uint_as_float(s[c2][i + 1]));
       } else {
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2)
+        for (int c2 = 0; c2 < NC; ++c2)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float x = (cbase + c2 * 32 + i <= lim) ? __uint_as_float(s[c2][i]) : -INFINITY;
@@ -337,12 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                        fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
-      // Combine the two halves' maxima (buffer double-buffered by tile parity).
-      // Only the two warps of a lane quarter meet here.
-      s_max[j & 1][half][r] = mt;
-      ok = group_sync(&bar_pair[quarter], pair_uses, STT_DEVERR_FWD_WAIT);
+      // Combine the parts' maxima (buffer double-buffered by tile parity);
+      // only the warps of one lane quarter meet here.
+      s_max[j & 1][part][r] = mt;
+      ok = group_sync(&bar_quad[quarter], quad_uses, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
-      mt = fmaxf(mt, s_max[j & 1][half ^ 1][r]);
+#pragma unroll
+      for (int p2 = 0; p2 < kParts; ++p2) mt = fmaxf(mt, s_max[j & 1][p2][r]);
 
       float alpha = 1.f;
       bool rescale_o = false;
@@ -356,13 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       // p = 2^(s sl2 - m): two elements per packed fp32x2 FMA, and the row sum
       // in four packed partial accumulators.
-      uint32_t pk[32];
+      uint32_t pk[NC * 16];
       const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
       uint64_t rp[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) rp[k] = f32x2(0.f, 0.f);
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2)
+      for (int c2 = 0; c2 < NC; ++c2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
@@ -385,29 +402,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = warp_wait(&bar_o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, STT_DEVERR_FWD_WAIT);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t ocol = tmem + lane_off + kColO + part * DH;
+        if constexpr (DH >= 32) {
 #pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          uint32_t o[32];
-          const uint32_t addr = tmem + lane_off + kColO + (half * (D / 64) + c2) * 32;
-          tmem_ld32(addr, o);
+          for (int c2 = 0; c2 < DH / 32; ++c2) {
+            uint32_t o[32];
+            tmem_ld32(ocol + c2 * 32, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(addr, o);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(ocol + c2 * 32, o);
+          }
+        } else {
+          uint32_t o[16];
+          tmem_ld16(ocol, o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(ocol, o);
         }
         tmem_st_wait();
       }
-      // P row half (bf16 pairs) over this half's own S columns: the A operand
-      // of O += P V.
-      {
-        const uint32_t pa = tmem + lane_off + kColS0 + sb * kTile + half * 64;
-        uint32_t p0[16], p1[16];
+      // P of this thread's keys (bf16 pairs) into the first columns of its own
+      // S columns: the A operand of O += P V.
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          p0[c] = pk[c];
-          p1[c] = pk[16 + c];
-        }
-        tmem_st16(pa, p0);
-        tmem_st16(pa + 16, p1);
+      for (int c2 = 0; c2 < NC; ++c2) {
+        uint32_t pp[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pp[c] = pk[c2 * 16 + c];
+        tmem_st16(scol + c2 * 16, pp);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -419,26 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
 
-    // This thread's half of the O row, in registers.
-    constexpr int DH = D / 2;
+    // This thread's DH columns of the O row, in registers.
     float o[DH];
     if (ok && n_kv > 0) {
+      const uint32_t ocol = tmem + lane_off + kColO + part * DH;
+      if constexpr (DH >= 32) {
 #pragma unroll
-      for (int c2 = 0; c2 < DH / 32; c2 += 2) {
-        uint32_t u0[32], u1[32];
-        const uint32_t a0 = tmem + lane_off + kColO + half * DH + c2 * 32;
-        if (DH / 32 >= 2) {
-          tmem_ld32x2(a0, a0 + 32, u0, u1);
+        for (int c2 = 0; c2 < DH / 32; ++c2) {
+          uint32_t u[32];
+          tmem_ld32(ocol + c2 * 32, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            o[c2 * 32 + i] = __uint_as_float(u0[i]);
-            if (c2 * 32 + 32 + i < DH) o[c2 * 32 + 32 + i] = __uint_as_float(u1[i]);
-          }
-        } else {
-          tmem_ld32(a0, u0);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = __uint_as_float(u0[i]);
+          for (int i = 0; i < 32; ++i) o[c2 * 32 + i] = __uint_as_float(u[i]);
         }
+      } else {
+        uint32_t u[16];
+        tmem_ld16(ocol, u);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = __uint_as_float(u[i]);
       }
     } else {
 #pragma unroll
@@ -447,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------- suffix keys (blocks 1..k) --
     // Query q < T sees key q of every later block: one score per block, a
-    // register-level online-softmax update of this thread's O half.
-    // The two threads of a row each take half of the score's dot product and
-    // exchange the halves through shared memory.
+    // register-level online-softmax update of this thread's O columns.
+    // The threads of a row each take their part of the score's dot product
+    // and exchange the parts through shared memory.
     const bool sfx_row = qrow < T;
     for (int w = 0; ok && w < n_sfx; ++w) {
       const int st = (n_kv + w) % kStages;
@@ -457,11 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const unsigned char* sK = smem + L::k0 + st * L::kKV;
       const unsigned char* sV = smem + L::v0 + st * L::kKV;
-      s_dot[w & 1][half][r] = sfx_row ? smem_half_row_dot<D>(sQ, sK, r, half) : 0.f;
+      s_dot[w & 1][part][r] = sfx_row ? smem_part_row_dot<D, kParts>(sQ, sK, r, part) : 0.f;
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
       if (!ok) break;
       if (sfx_row) {
-        const float sj = (s_dot[w & 1][0][r] + s_dot[w & 1][1][r]) * sl2;
+        float dsum = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < kParts; ++p2) dsum += s_dot[w & 1][p2][r];
+        const float sj = dsum * sl2;
         if (sj > m_run) {
           const float alpha = ex2(m_run - sj);  // 0 when m_run is -inf
           l_run *= alpha;
@@ -470,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = sj;
         }
         const float pj = ex2(sj - m_run);
-        if (half == 0) l_run += pj;
+        if (part == 0) l_run += pj;
 #pragma unroll
         for (int c = 0; c < DH / 8; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4*>(sV + swz_chunk_offset(r, half * (DH / 8) + c, kTile));
+          const uint4 x = *reinterpret_cast<const uint4*>(sV + swz_chunk_offset(r, part * (DH / 8) + c, kTile));
           o[c * 8 + 0] = fmaf(pj, bf16lo(x.x), o[c * 8 + 0]);
           o[c * 8 + 1] = fmaf(pj, bf16hi(x.x), o[c * 8 + 1]);
           o[c * 8 + 2] = fmaf(pj, bf16lo(x.y), o[c * 8 + 2]);
@@ -489,9 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ----------------------------------------------------------- epilogue --
     if (ok) {
-      s_sum[half][r] = l_run;
+      s_sum[part][r] = l_run;
       ok = group_sync(&bar_grp, grp_uses, STT_DEVERR_FWD_WAIT);
-      l_run += s_sum[half ^ 1][r];
+      l_run = 0.f;
+#pragma unroll
+      for (int p2 = 0; p2 < kParts; ++p2) l_run += s_sum[p2][r];
     }
     if (ok) {
       // O (bf16) is staged in the Q buffer, which every reader is done with
@@ -501,12 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
       for (int c = 0; c < DH / 8; ++c)
-        *reinterpret_cast<uint4*>(sQ + swz_chunk_offset(r, half * (DH / 8) + c, kTile)) =
+        *reinterpret_cast<uint4*>(sQ + swz_chunk_offset(r, part * (DH / 8) + c, kTile)) =
             make_uint4(pack_bf16(o[c * 8 + 0] * inv_l, o[c * 8 + 1] * inv_l),
                        pack_bf16(o[c * 8 + 2] * inv_l, o[c * 8 + 3] * inv_l),
                        pack_bf16(o[c * 8 + 4] * inv_l, o[c * 8 + 5] * inv_l),
                        pack_bf16(o[c * 8 + 6] * inv_l, o[c * 8 + 7] * inv_l));
-      if (half == 0 && qrow < P.Q_LEN)
+      if (part == 0 && qrow < P.Q_LEN)
         P.lse[(size_t)bh * P.Q_LEN + qrow] =
             l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       fence_proxy_async_smem();
