@@ -201,6 +201,8 @@ STT_API int stt_profile_stop(int* n, int* kernel_ids, float* ms, int capacity);
 STT_API const char* stt_kernel_name(int kernel_id);
 
 #define STT_KERNEL_SOFT_CE 1
+/* The soft-CE row kernel and its loss sum are recorded together as
+ * STT_KERNEL_SOFT_CE; STT_KERNEL_SOFT_CE_LOSS_SUM only names the second. */
 #define STT_KERNEL_SOFT_CE_LOSS_SUM 2
 #define STT_KERNEL_ATTN_FWD 3
 #define STT_KERNEL_ATTN_BWD_PREP 4

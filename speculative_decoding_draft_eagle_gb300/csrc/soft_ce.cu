@@ -345,6 +345,8 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
   // Every CTA's mbarriers are initialised before any CTA pushes to them.
   cluster_arrive_release();
   cluster_wait_acquire();
+  // The loss sum may be scheduled now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kPWarps) {
     // Producer: the slices of the cluster's rows with g != 0, in order.
@@ -535,9 +537,13 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
 }
 
 // Fixed-order sum of the per-row weighted losses (one CTA, deterministic).
+// Launched as a programmatic dependent of the row kernel, so its launch
+// overlaps the row kernel's tail; it reads wl only after that grid has
+// completed and its writes are visible (griddepcontrol.wait).
 __global__ void __launch_bounds__(1024) soft_ce_loss_sum(const float* wl, long long N,
                                                          float* loss) {
   __shared__ double part[1024];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   double acc = 0.0;
   for (long long i = threadIdx.x; i < N; i += 1024) acc += (double)wl[i];
   part[threadIdx.x] = acc;
@@ -676,8 +682,10 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
     cfg.numAttrs = 1;
     prof_before(s, STT_KERNEL_SOFT_CE);
     cudaError_t e = cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel, P);
-    prof_after(s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      prof_after(s);
+      return e;
+    }
   } else if (N > 0) {
     // One cluster per row (also taken if the persistent kernel cannot be resident).
     const CePlan fb = plan.persistent ? soft_ce_plan_cta(z, p, V) : plan;
@@ -705,12 +713,29 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
     cfg.numAttrs = 1;
     prof_before(s, STT_KERNEL_SOFT_CE);
     e = cudaLaunchKernelEx(&cfg, kern, P);
-    prof_after(s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      prof_after(s);
+      return e;
+    }
+  } else {
+    prof_before(s, STT_KERNEL_SOFT_CE);
   }
-  prof_before(s, STT_KERNEL_SOFT_CE_LOSS_SUM);
-  soft_ce_loss_sum<<<1, 1024, 0, s>>>(wl, (long long)N, loss);
+  // The loss sum follows the row kernel directly (no profiling event between
+  // them, which would serialise the pair), as a programmatic dependent launch;
+  // the profiled unit STT_KERNEL_SOFT_CE covers both kernels.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(1, 1, 1);
+  lc.blockDim = dim3(1024, 1, 1);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  const cudaError_t e2 = cudaLaunchKernelEx(&lc, soft_ce_loss_sum, wl, (long long)N, loss);
   prof_after(s);
+  if (e2 != cudaSuccess) return e2;
   return cudaGetLastError();
 }
 
