@@ -39,6 +39,7 @@ constexpr int kThreads = 480;
 constexpr int kCompute = 256;
 constexpr int kComputeWarps = kCompute / 32;  // barriers count one arrival per warp
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpMma2 = 14;
+constexpr int kHeadChunk = 16;  // heads per group of key-tile CTAs scheduled together
 constexpr int kEpiWarps = 4;  // one per TMEM lane quarter (warp % 4)
 
 struct BwdParams {
@@ -335,9 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float s_stat[2][2][kTile];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Heads are taken in chunks of kHeadChunk: the CTAs of one chunk run
+  // together and re-read only their heads' Q and dO (16 heads x 2 x Q_LEN x D
+  // bf16 stay in L2), and within a chunk the key tiles go longest first.
   const int nb = P.H * P.B;
-  const int c = (int)(blockIdx.x / nb);  // key tile; low tiles see the most query tiles
-  const int bh = (int)(blockIdx.x % nb);
+  const int ch = nb < kHeadChunk ? nb : kHeadChunk;
+  const int chunk = (int)(blockIdx.x / (unsigned)(P.n_t * ch));
+  const int chunk_heads = min(ch, nb - chunk * ch);
+  const int rem = (int)blockIdx.x - chunk * P.n_t * ch;
+  const int c = rem / chunk_heads;  // key tile; low tiles see the most query tiles
+  const int bh = chunk * ch + rem % chunk_heads;
   const int b = bh / P.H, h = bh % P.H, hk = h / P.G;
   const int c0 = c * kTile;
   const int T = P.T[b];
