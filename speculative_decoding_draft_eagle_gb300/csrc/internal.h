@@ -15,6 +15,7 @@ struct CePlan {
   int slice;     // elements of a row per CTA
   int smem;      // dynamic shared memory bytes per CTA
   bool persistent;  // persistent clusters walking the rows, nb row buffers per CTA
+  bool split;       // persistent with z and p in separate buffers (large slices)
   int nb;
 };
 CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V);

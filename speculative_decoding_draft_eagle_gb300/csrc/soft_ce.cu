@@ -19,7 +19,7 @@
 //   * Per-row weighted losses g_r * loss_r go to the workspace; a one-CTA kernel
 //     sums them in a fixed order, so the scalar loss is deterministic.
 // Two kernels implement this.  soft_ce_persistent_kernel (16-byte aligned rows,
-// slices of at most kPSliceMax elements) keeps one cluster per group of SMs
+// slices of at most kPSliceMaxSplit elements) keeps one cluster per group of SMs
 // resident and pipelines rows through it; soft_ce_kernel (any row, one cluster
 // per row) covers the rest.
 #include <cmath>
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) soft_ce_kernel(const CeParams P) {
 }
 
 // ---------------------------------------------------------------------------
-// Persistent variant (bulk path, V up to kPSliceMax * kMaxCluster).
+// Persistent variant (bulk path, V up to kPSliceMaxSplit * kMaxCluster).
 //
 // A cluster of C CTAs (one per SM) walks the rows cid, cid + ncl, ... where
 // ncl is the number of co-resident clusters.  Each CTA owns one slice of every
@@ -291,6 +291,13 @@ constexpr int kPMinBufs = 2;
 constexpr int kPMaxBufs = 2;
 constexpr int kPSmemBudget = 200 * 1024;  // shared bytes for the row buffers
 constexpr int kPSliceMax = kPConsumers * kPVec * 4;
+// Larger slices (vocabularies past 16 x 7168) keep only exp(z - m_w) in
+// registers (kPVecSplit float4 per thread) and read p from shared memory again
+// for the gradient: z has two buffers (free once reduced), p three (free once
+// the gradient is written).
+constexpr int kPVecSplit = 10;
+constexpr int kPSliceMaxSplit = kPConsumers * kPVecSplit * 4;  // 10240
+static_assert(20 * kPSliceMaxSplit <= kPSmemBudget, "split buffers for the largest slice");
 constexpr int kPParts = kMaxCluster * kPWarps;  // warp partials of one row, at most
 static_assert(kPSliceMax * 8 * kPMinBufs <= kPSmemBudget, "buffers for the largest slice");
 
@@ -306,19 +313,25 @@ struct CePParams {
   int nb;
 };
 
-// One row's slice as a consumer thread keeps it between reduce and finish.
+// One row's slice as a consumer thread keeps it between reduce and finish
+// (p only when it is not kept in shared memory).
+template <int VEC, bool HAS_P>
 struct CeRowRegs {
-  float4 e[kPVec];  // exp(z - m_w)
-  float4 p[kPVec];
+  float4 e[VEC];  // exp(z - m_w)
+  float4 p[HAS_P ? VEC : 1];
   long long row;
   float g;
-  float m;          // the warp's max m_w
+  float m;        // the warp's max m_w
 };
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const CePParams P) {
+  constexpr int VEC = SPLIT ? kPVecSplit : kPVec;
+  using Row = CeRowRegs<VEC, !SPLIT>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ uint64_t full[kPMaxBufs];
   __shared__ uint64_t empty[kPMaxBufs];
+  __shared__ uint64_t pfull[3], pempty[3];  // p buffers of the split layout
   __shared__ uint64_t xbar[4];
   __shared__ __align__(16) float4 stats[4][kPParts];
 
@@ -331,14 +344,24 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
   const long long rem = P.V - begin;
   const int len = rem <= 0 ? 0 : (rem < P.slice ? (int)rem : P.slice);
   const int n4 = len >> 2;
-  const int nb = P.nb;
+  const int nb = SPLIT ? 2 : P.nb;  // z (and, unsplit, p) buffers
   float* const sbase = reinterpret_cast<float*>(smem_raw);
+  // Buffer b of z (and of p when unsplit); p buffer c of the split layout.
+  auto zbuf = [&](int b) { return sbase + (size_t)b * (SPLIT ? 1 : 2) * P.slice; };
+  auto pbuf = [&](int b, int c) {
+    return SPLIT ? sbase + (size_t)(2 + c) * P.slice : sbase + (size_t)b * 2 * P.slice + P.slice;
+  };
 
   if (tid == 0) {
     for (int b = 0; b < nb; ++b) {
       mbar_init(&full[b], 1);
       mbar_init(&empty[b], kPWarps);
     }
+    if (SPLIT)
+      for (int c = 0; c < 3; ++c) {
+        mbar_init(&pfull[c], 1);
+        mbar_init(&pempty[c], kPWarps);
+      }
     for (int k = 0; k < 4; ++k) mbar_init(&xbar[k], 1);
     fence_mbar_init();
   }
@@ -359,14 +382,27 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
         if (gcur == 0.0f) continue;
         const int b = j % nb;
         if (j >= nb) mbar_wait(&empty[b], (uint32_t)(j / nb - 1) & 1u, STT_DEVERR_CE_WAIT);
-        float* zs = sbase + (size_t)b * 2 * P.slice;
+        float* zs = zbuf(b);
         const float* zsrc = P.z + r * P.V + begin;
         const float* psrc = P.p + r * P.V + begin;
-        mbar_arrive_expect_tx(&full[b], 8u * (uint32_t)len);
-        for (int c = 0; c < len; c += kChunk) {
-          const uint32_t bytes = (uint32_t)min(kChunk, len - c) * 4u;
-          bulk_load(zs + c, zsrc + c, bytes, &full[b]);
-          bulk_load(zs + P.slice + c, psrc + c, bytes, &full[b]);
+        if (SPLIT) {
+          mbar_arrive_expect_tx(&full[b], 4u * (uint32_t)len);
+          for (int c = 0; c < len; c += kChunk)
+            bulk_load(zs + c, zsrc + c, (uint32_t)min(kChunk, len - c) * 4u, &full[b]);
+          const int pc = j % 3;
+          if (j >= 3) mbar_wait(&pempty[pc], (uint32_t)(j / 3 - 1) & 1u, STT_DEVERR_CE_WAIT);
+          float* ps = pbuf(b, pc);
+          mbar_arrive_expect_tx(&pfull[pc], 4u * (uint32_t)len);
+          for (int c = 0; c < len; c += kChunk)
+            bulk_load(ps + c, psrc + c, (uint32_t)min(kChunk, len - c) * 4u, &pfull[pc]);
+        } else {
+          float* ps = pbuf(b, 0);
+          mbar_arrive_expect_tx(&full[b], 8u * (uint32_t)len);
+          for (int c = 0; c < len; c += kChunk) {
+            const uint32_t bytes = (uint32_t)min(kChunk, len - c) * 4u;
+            bulk_load(zs + c, zsrc + c, bytes, &full[b]);
+            bulk_load(ps + c, psrc + c, bytes, &full[b]);
+          }
         }
         ++j;
       }
@@ -374,7 +410,7 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     __syncwarp();
   } else {
     // Consumers.
-    CeRowRegs ra, rb;
+    Row ra, rb;
     long long row = cid;
     float g_row = cid < P.N ? __ldg(P.g + cid) : 0.0f;
     int v = 0;  // valid rows reduced so far
@@ -386,7 +422,7 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
         float* zrow = P.z + row * P.V + begin;
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < kPVec; ++k) {
+        for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
           if (i < n4) st_global_cs_f4(zrow + 4 * i, zero);
         }
@@ -401,10 +437,10 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     };
 
     // reduce(v) of the current row into `cur`, then push the warp partial.
-    auto reduce = [&](CeRowRegs& cur) {
+    auto reduce = [&](Row& cur) {
       const int b = v % nb;
-      const float4* zs4 = reinterpret_cast<const float4*>(sbase + (size_t)b * 2 * P.slice);
-      const float4* ps4 = reinterpret_cast<const float4*>(sbase + (size_t)b * 2 * P.slice + P.slice);
+      const float4* zs4 = reinterpret_cast<const float4*>(zbuf(b));
+      const float4* ps4 = reinterpret_cast<const float4*>(pbuf(b, v % 3));
       cur.row = row;
       cur.g = g_row;
       row += ncl;
@@ -412,18 +448,19 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
       float m = -INFINITY;
       if (len > 0) {
         mbar_wait(&full[b], (uint32_t)(v / nb) & 1u, STT_DEVERR_CE_WAIT);
+        if (SPLIT) mbar_wait(&pfull[v % 3], (uint32_t)(v / 3) & 1u, STT_DEVERR_CE_WAIT);
 #pragma unroll
-        for (int k = 0; k < kPVec; ++k) {
+        for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
           if (i < n4) {
             cur.e[k] = zs4[i];
-            cur.p[k] = ps4[i];
+            if constexpr (!SPLIT) cur.p[k] = ps4[i];
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[b]);  // this warp is done with buffer b
 #pragma unroll
-        for (int k = 0; k < kPVec; ++k) {
+        for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
           if (i < n4)
             m = fmaxf(m, fmaxf(fmaxf(cur.e[k].x, cur.e[k].y), fmaxf(cur.e[k].z, cur.e[k].w)));
@@ -435,11 +472,15 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
       if (m != -INFINITY) {
         const float mb = m * kLog2e;
 #pragma unroll
-        for (int k = 0; k < kPVec; ++k) {
+        for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
           if (i < n4) {
             const float4 zv = cur.e[k];
-            const float4 pv = cur.p[k];
+            float4 pv;
+            if constexpr (SPLIT)
+              pv = ps4[i];
+            else
+              pv = cur.p[k];
             float4 e;
             e.x = ex2(fmaf(zv.x, kLog2e, -mb));
             e.y = ex2(fmaf(zv.y, kLog2e, -mb));
@@ -465,7 +506,7 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     };
 
     // finish(u) of the row kept in `prv`.
-    auto finish = [&](const CeRowRegs& prv, int u) {
+    auto finish = [&](const Row& prv, int u) {
       mbar_wait_cluster(&xbar[u & 3], (uint32_t)(u >> 2) & 1u, STT_DEVERR_CE_WAIT);
       const int np = C * kPWarps;
       float4 q[kPParts / 32];
@@ -492,17 +533,27 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
       // exp(z - lse) g Sp = e exp(m_w - lse) g Sp; m_w <= lse, so this cannot overflow.
       const float scale = (prv.m == -INFINITY) ? 0.f : ex2((prv.m - lse) * kLog2e) * (g * Sp);
       float* zrow = P.z + prv.row * P.V + begin;
+      const float4* ps4 = reinterpret_cast<const float4*>(pbuf(0, u % 3));
 #pragma unroll
-      for (int k = 0; k < kPVec; ++k) {
+      for (int k = 0; k < VEC; ++k) {
         const int i = tid + k * kPConsumers;
         if (i < n4) {
+          float4 pv;
+          if constexpr (SPLIT)
+            pv = ps4[i];
+          else
+            pv = prv.p[k];
           float4 o;
-          o.x = fmaf(prv.e[k].x, scale, -prv.p[k].x * g);
-          o.y = fmaf(prv.e[k].y, scale, -prv.p[k].y * g);
-          o.z = fmaf(prv.e[k].z, scale, -prv.p[k].z * g);
-          o.w = fmaf(prv.e[k].w, scale, -prv.p[k].w * g);
+          o.x = fmaf(prv.e[k].x, scale, -pv.x * g);
+          o.y = fmaf(prv.e[k].y, scale, -pv.y * g);
+          o.z = fmaf(prv.e[k].z, scale, -pv.z * g);
+          o.w = fmaf(prv.e[k].w, scale, -pv.w * g);
           st_global_cs_f4(zrow + 4 * i, o);
         }
+      }
+      if (SPLIT && len > 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[u % 3]);  // this warp is done with p of row u
       }
       if (rank == 0 && tid == 0) {
         const float ell = fmaf(lse, Sp, -Spz);
@@ -578,6 +629,7 @@ CePlan soft_ce_plan_cta(const float* z, const float* p, int64_t V) {
   plan.slice = (int)slice;
   plan.smem = (int)(8 * slice);
   plan.persistent = false;
+  plan.split = false;
   plan.nb = 1;
   return plan;
 }
@@ -589,17 +641,24 @@ CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
   CePlan plan = soft_ce_plan_cta(z, p, V);
   if (plan.bulk) {
     // Persistent clusters: slices of about kPSliceTarget elements, at least
-    // kPMinBufs row buffers per CTA.
-    long long Cp = (V + kPSliceTarget - 1) / kPSliceTarget;
-    const long long Cmin = (V + kPSliceMax - 1) / kPSliceMax;
-    if (Cp < Cmin) Cp = Cmin;
-    if (Cp < 1) Cp = 1;
-    if (Cp > kMaxCluster) Cp = kMaxCluster;
-    long long sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
-    while (Cp > 1 && (Cp - 1) * sl >= V) {
-      --Cp;
-      sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
-    }
+    // kPMinBufs row buffers per CTA; slices past kPSliceMax take the split
+    // layout (z and p in separate buffers, p read again from shared memory).
+    auto split = [&](long long slice_max, long long* C_out, long long* sl_out) {
+      long long Cp = (V + kPSliceTarget - 1) / kPSliceTarget;
+      const long long Cmin = (V + slice_max - 1) / slice_max;
+      if (Cp < Cmin) Cp = Cmin;
+      if (Cp < 1) Cp = 1;
+      if (Cp > kMaxCluster) Cp = kMaxCluster;
+      long long sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
+      while (Cp > 1 && (Cp - 1) * sl >= V) {
+        --Cp;
+        sl = ((V + Cp - 1) / Cp + 3) / 4 * 4;
+      }
+      *C_out = Cp;
+      *sl_out = sl;
+    };
+    long long Cp, sl;
+    split(kPSliceMax, &Cp, &sl);
     long long nb = kPSmemBudget / (8 * sl);
     if (nb > kPMaxBufs) nb = kPMaxBufs;
     if (sl <= kPSliceMax && nb >= kPMinBufs) {
@@ -608,6 +667,16 @@ CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
       plan.slice = (int)sl;
       plan.nb = (int)nb;
       plan.smem = (int)(nb * 8 * sl);
+    } else {
+      split(kPSliceMaxSplit, &Cp, &sl);
+      if (sl <= kPSliceMaxSplit) {
+        plan.persistent = true;
+        plan.split = true;
+        plan.C = (int)Cp;
+        plan.slice = (int)sl;
+        plan.nb = 2;
+        plan.smem = (int)(20 * sl);  // two z buffers, three p buffers
+      }
     }
   }
   return plan;
@@ -615,8 +684,10 @@ CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
 
 namespace {
 
-// Co-resident clusters of the persistent kernel for (C, smem) on the current
-// device; 0 if the query fails.  Cached per device for the last configuration.
+// Co-resident clusters of soft_ce_persistent_kernel<SPLIT> for (C, smem) on
+// the current device; 0 if the query fails.  Cached per device (and SPLIT) for
+// the last configuration.
+template <bool SPLIT>
 int persistent_clusters(int C, int smem) {
   static std::mutex mu;
   static int cache_dev[64], cache_C[64], cache_smem[64], cache_n[64];
@@ -629,10 +700,10 @@ int persistent_clusters(int C, int smem) {
     init = true;
   }
   if (cache_dev[dev] == dev && cache_C[dev] == C && cache_smem[dev] == smem) return cache_n[dev];
-  if (cudaFuncSetAttribute(soft_ce_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(soft_ce_persistent_kernel<SPLIT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
-  if (C > 8 && cudaFuncSetAttribute(soft_ce_persistent_kernel,
+  if (C > 8 && cudaFuncSetAttribute(soft_ce_persistent_kernel<SPLIT>,
                                     cudaFuncAttributeNonPortableClusterSizeAllowed,
                                     1) != cudaSuccess)
     return 0;
@@ -648,7 +719,7 @@ int persistent_clusters(int C, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, soft_ce_persistent_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, soft_ce_persistent_kernel<SPLIT>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -664,7 +735,10 @@ int persistent_clusters(int C, int smem) {
 cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const float* g,
                            int64_t N, int64_t V, float* row_loss, float* loss, float* wl,
                            cudaStream_t s) {
-  const int ncl = (N > 0 && plan.persistent) ? persistent_clusters(plan.C, plan.smem) : 0;
+  int ncl = 0;
+  if (N > 0 && plan.persistent)
+    ncl = plan.split ? persistent_clusters<true>(plan.C, plan.smem)
+                     : persistent_clusters<false>(plan.C, plan.smem);
   if (ncl > 0) {
     const long long n_clusters = ncl < N ? ncl : N;
     CePParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, plan.C, plan.slice, plan.nb};
@@ -681,7 +755,8 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_before(s, STT_KERNEL_SOFT_CE);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel, P);
+    cudaError_t e = plan.split ? cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel<true>, P)
+                               : cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel<false>, P);
     if (e != cudaSuccess) {
       prof_after(s);
       return e;
