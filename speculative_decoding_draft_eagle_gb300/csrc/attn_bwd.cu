@@ -141,26 +141,35 @@ __device__ __forceinline__ uint32_t swz128(int r, int w) {
 // size (the loops over heads are unrolled so per-head values stay in
 // registers); G <= GM.
 // Register budget per group size: the per-head q, dO and dq values grow with
-// GM, so larger groups run fewer, fatter warps per SM.
+// the heads a thread holds, so larger groups run fewer, fatter warps per SM.
+// Groups of eight split their heads between the two half-warps (SH = 2): each
+// thread holds four heads, the half-warps combine their dK_j / dV_j partial
+// sums with one shuffle, and a warp covers half as many rows.
 template <int GM>
 struct PrepShape {
   static constexpr int E = 8;                               // 16-byte accesses
-  static constexpr int kJ = GM <= 2 ? 4 : (GM <= 4 ? 2 : 1);  // suffix blocks loaded together
-  static constexpr int kThreads = GM <= 2 ? 256 : 128;
-  static constexpr int kMinBlocks = GM <= 2 ? 2 : (GM <= 4 ? 3 : 2);
+  static constexpr int SH = GM >= 8 ? 2 : 1;                // half-warps sharing a row's heads
+  static constexpr int GH = GM / SH;                        // heads per thread
+  static constexpr int kJ = GH <= 2 ? 4 : 2;                // suffix blocks loaded together
+  static constexpr int kThreads = GH <= 2 ? 256 : 128;
+  static constexpr int kMinBlocks = GH <= 2 ? 2 : 3;
 };
 
 template <int D, int GM>
 __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBlocks)
     attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
   constexpr int E = PrepShape<GM>::E;
+  constexpr int SH = PrepShape<GM>::SH;
+  constexpr int GH = PrepShape<GM>::GH;
   constexpr int kJ = PrepShape<GM>::kJ;
-  constexpr int L = D / E;     // lanes per row
-  constexpr int RPW = 32 / L;  // rows per warp
+  constexpr int L = D / E;            // lanes per row
+  constexpr int RPW = 32 / SH / L;    // rows per warp
   constexpr int kWarps = PrepShape<GM>::kThreads / 32;
   using V = Bf16Vec<E>;
   const int lane = threadIdx.x & 31;
-  const int sub = lane / L, li = lane % L;
+  const int hh = lane / (32 / SH);    // which heads of the group: [hh GH, hh GH + GH)
+  const int lane_h = lane % (32 / SH);
+  const int sub = lane_h / L, li = lane_h % L;
   const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
   const long long stride = (long long)gridDim.x * kWarps * RPW;
   const int G = P.G;
@@ -176,16 +185,16 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
     const bool valid = live && q < P.T[b];  // rows with suffix keys
     const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + li * E;
 
-    V qv[GM], dov[GM];
-    float dq[GM][E], lse2[GM], dl[GM];
+    V qv[GH], dov[GH];
+    float dq[GH][E], lse2[GH], dl[GH];
     {
-      V ov[GM];
+      V ov[GH];
 #pragma unroll
-      for (int i = 0; i < GM; ++i) {
+      for (int i = 0; i < GH; ++i) {
         qv[i] = dov[i] = ov[i] = zero_vec<E>();
         lse2[i] = 0.f;
-        if (i < G && live) {
-          const size_t rq = (size_t)(b * P.H + hk * G + i) * P.Q_LEN + q;
+        if (hh * GH + i < G && live) {
+          const size_t rq = (size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q;
           const size_t off = rq * D + li * E;
           dov[i] = ldg_vec<E>(P.dout + off);
           ov[i] = ldg_vec<E>(P.out + off);
@@ -193,13 +202,14 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
           lse2[i] = P.lse[rq] * kLog2e;
         }
       }
+      // The group sums shuffle across the whole warp, so every lane runs them
+      // for every head slot; slots past the group's heads hold zeros and add
+      // nothing.
 #pragma unroll
-      for (int i = 0; i < GM; ++i) {
-        dl[i] = 0.f;
-        if (i < G) {
-          dl[i] = group_sum<L>(dot_vec<E>(dov[i], ov[i]));
-          if (live && li == 0) P.delta[(size_t)(b * P.H + hk * G + i) * P.Q_LEN + q] = dl[i];
-        }
+      for (int i = 0; i < GH; ++i) {
+        dl[i] = group_sum<L>(dot_vec<E>(dov[i], ov[i]));
+        if (hh * GH + i < G && live && li == 0)
+          P.delta[(size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q] = dl[i];
 #pragma unroll
         for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
       }
@@ -223,22 +233,34 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
 #pragma unroll
         for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
 #pragma unroll
-        for (int i = 0; i < GM; ++i) {
-          if (i < G) {
-            const float s = group_sum<L>(dot_vec<E>(qv[i], kv[u]));
-            const float dp = group_sum<L>(dot_vec<E>(dov[i], vv[u]));
-            // Rows without suffix keys get no contribution (their lse may be -inf).
-            const float p = valid ? ex2(s * P.scale_log2 - lse2[i]) : 0.f;
-            const float dss = p * (dp - dl[i]) * P.scale;
+        for (int i = 0; i < GH; ++i) {
+          // Head slots past the group's heads: qv = dov = 0 and Delta = 0, so
+          // dss = 0 and p dO = 0 (the sums still run on every lane).
+          const float s = group_sum<L>(dot_vec<E>(qv[i], kv[u]));
+          const float dp = group_sum<L>(dot_vec<E>(dov[i], vv[u]));
+          // Rows without suffix keys get no contribution (their lse may be -inf).
+          const float p = valid ? ex2(s * P.scale_log2 - lse2[i]) : 0.f;
+          const float dss = p * (dp - dl[i]) * P.scale;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              dq[i][e] = fmaf(dss, vec_at<E>(kv[u], e), dq[i][e]);
-              dk[e] = fmaf(dss, vec_at<E>(qv[i], e), dk[e]);
-              dv[e] = fmaf(p, vec_at<E>(dov[i], e), dv[e]);
-            }
+          for (int e = 0; e < E; ++e) {
+            dq[i][e] = fmaf(dss, vec_at<E>(kv[u], e), dq[i][e]);
+            dk[e] = fmaf(dss, vec_at<E>(qv[i], e), dk[e]);
+            dv[e] = fmaf(p, vec_at<E>(dov[i], e), dv[e]);
           }
         }
-        if (live) {
+        if constexpr (SH == 2) {
+          // The other half-warp holds the group's other heads: sum, then
+          // half-warp 0 stores dK_j and half-warp 1 dV_j.
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            dk[e] += __shfl_xor_sync(0xffffffffu, dk[e], 16);
+            dv[e] += __shfl_xor_sync(0xffffffffu, dv[e], 16);
+          }
+          float out[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) out[e] = hh == 0 ? dk[e] : dv[e];
+          if (live) store_vec<E>((hh == 0 ? P.dkb[j] : P.dvb[j]) + kvoff, out, true);
+        } else if (live) {
           store_vec<E>(P.dkb[j] + kvoff, dk, true);
           store_vec<E>(P.dvb[j] + kvoff, dv, true);
         }
@@ -246,14 +268,15 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
     }
     if (live) {
 #pragma unroll
-      for (int i = 0; i < GM; ++i)
-        if (i < G)
-          store_vec<E>(P.dq + ((size_t)(b * P.H + hk * G + i) * P.Q_LEN + q) * D + li * E, dq[i], false);
+      for (int i = 0; i < GH; ++i)
+        if (hh * GH + i < G)
+          store_vec<E>(P.dq + ((size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q) * D + li * E,
+                       dq[i], false);
       float z[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) z[e] = 0.f;
-      store_vec<E>(P.dkb[0] + kvoff, z, false);
-      store_vec<E>(P.dvb[0] + kvoff, z, false);
+      if (SH == 1 || hh == 0) store_vec<E>(P.dkb[0] + kvoff, z, false);
+      if (SH == 1 || hh == 1) store_vec<E>(P.dvb[0] + kvoff, z, false);
     }
   }
 }
@@ -788,7 +811,7 @@ template <int D, int GM>
 void launch_prep(const BwdParams& P, cudaStream_t s) {
   const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
   using S = PrepShape<GM>;
-  const long long per_block = (S::kThreads / 32) * (32 / (D / S::E));
+  const long long per_block = (S::kThreads / 32) * (32 / S::SH / (D / S::E));
   long long blocks = (rows + per_block - 1) / per_block;
   if (blocks > 152 * 64) blocks = 152 * 64;  // grid-stride beyond that
   attn_bwd_prep_kernel<D, GM><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
