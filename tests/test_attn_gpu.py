@@ -87,6 +87,7 @@ FWD_CASES = [
     (1, 8, 2, 384, 128, 12, [1]),          # T = 1, long TTT
     (3, 2, 2, 130, 128, 2, [129, 130, 2]),
     (1, 4, 4, 64, 64, 1, [50]),            # Q_LEN smaller than one tile
+    (3, 8, 2, 384, 128, 1, [384, 200, 7]),  # 24 heads: key-tile CTAs in a full and a partial head chunk
     (2, 8, 1, 512, 128, 6, [511, 300]),    # group of 8 query heads
     (1, 6, 2, 256, 128, 2, [200]),         # group of 3 (below the unrolled bound of 4)
     (1, 6, 1, 192, 128, 5, [150]),         # group of 6 (below the unrolled bound of 8)
