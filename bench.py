@@ -5,13 +5,16 @@ One step = the whole hot path over one batch of synthetic input: for every TTT
 step k of the workload, sparse-tree attention forward and backward, then the
 in-place soft-CE over the workload's logits.  Inputs are resident in HBM when
 the timed region starts; every timed step consumes its own fresh copy of the
-logits (the soft-CE overwrites them).
+logits (the soft-CE overwrites them), refilled outside the timed region.
 
 Prints ONE JSON line (rank 0).  `value` is the attention fwd+bwd useful
-TFLOP/s (only unmasked score entries, 4*D flops forward and 10*D backward);
-`soft_ce` carries the soft-CE's algorithmic GB/s.
+TFLOP/s (only unmasked score entries, 4*D flops forward and 10*D backward) of
+the headline workload (long_ttt: B1 H32 Hkv8 D128 Q_LEN 8192, TTT steps
+0..12, the largest single-GPU workload); `soft_ce` carries the soft-CE's
+algorithmic GB/s; `other_workloads` the same figures for the other full-size
+workloads (fewer steps).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama8b]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_ttt]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 """
 
@@ -22,7 +25,6 @@ import csv
 import hashlib
 import io
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -42,28 +44,42 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "speculative_decoding_draft_eagle_gb300", "csrc")
 METRIC = "TTT-attn fwd+bwd useful TFLOP/s; in-place soft-CE GB/s (1×GB300)"
+HEADLINE = "long_ttt"
+Z_BUDGET = 40e9  # bytes of device memory for fresh logits copies
 
-# kernel id -> (source file, roofline bound)
-KERNELS = {1: ("soft_ce.cu", "hbm"), 2: ("soft_ce.cu", "hbm"), 3: ("attn_fwd.cu", "tensor"),
-           4: ("attn_bwd.cu", "hbm"), 5: ("attn_bwd.cu", "tensor")}
+# kernel name -> (source file, roofline bound)
+KERNELS = {"soft_ce": ("soft_ce.cu", "hbm"), "attn_fwd": ("attn_fwd.cu", "tensor"),
+           "attn_bwd_prep": ("attn_bwd.cu", "hbm"), "attn_bwd_causal": ("attn_bwd.cu", "tensor")}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b", choices=[n for n in wl.WORKLOADS if n != "tiny"])
+    ap.add_argument("--workload", default=HEADLINE, choices=[n for n in wl.WORKLOADS if n != "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-other-workloads", action="store_true")
+    ap.add_argument("--other-steps", type=int, default=5)
+    a = ap.parse_args()
+    if a.warmup < 0 or a.steps < 1:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    return a
 
 
 # ------------------------------------------------------------ distributed --
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
+
+
+def check_world(a):
+    _, world, _ = dist_env()
+    if a.gpus != world:
+        raise SystemExit(f"--gpus {a.gpus} but WORLD_SIZE={world}: launch N > 1 with "
+                         f"torch.distributed.run --nproc-per-node {a.gpus}")
 
 
 def dist_init(backend):
@@ -81,21 +97,12 @@ def barrier(world):
         dist.barrier()
 
 
-def allreduce_max(x: float, world, device) -> float:
+def allreduce(x: float, world, device, op) -> float:
     if world == 1:
         return x
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def allreduce_sum(x: float, world, device) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -103,11 +110,9 @@ def allreduce_sum(x: float, world, device) -> float:
 def peaks():
     try:
         d = json.load(open(PEAKS_FILE))
-        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
-                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                "src": "measured"}
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]), "src": "measured"}
     except Exception:
-        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+        return {"hbm": 6800.0, "bf16": 1900.0, "src": "fallback"}
 
 
 def source_hash(fname):
@@ -119,13 +124,12 @@ def source_hash(fname):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_name, src_file, workload):
+def traffic_for(kernel_name, workload):
     """DRAM bytes per launch from a committed ncu capture, if the kernel's source
     is unchanged since the capture (else None)."""
     try:
-        d = json.load(open(TRAFFIC_FILE))
-        e = d[workload][kernel_name]
-        if e.get("source_hash") != source_hash(src_file):
+        e = json.load(open(TRAFFIC_FILE))[workload][kernel_name]
+        if e.get("source_hash") != source_hash(KERNELS[kernel_name][0]):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -176,7 +180,151 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- our arm -----
+class Workbench:
+    """Device-resident inputs and outputs of one workload, and one step of the path."""
+
+    def __init__(self, name, dev, seed, n_steps):
+        from speculative_decoding_draft_eagle_gb300 import ops
+        self.ops = ops
+        self.name = name
+        w = wl.WORKLOADS[name]
+        self.sh, self.sc = sh, sc = w.attn, w.soft_ce
+        self.T, self.Ks, self.Vs, self.qs, self.dOs = wl.attn_inputs(sh, dev, seed)
+        self.z0, self.p, self.g = wl.soft_ce_inputs(sc, dev, seed, T=self.T, Q_LEN=sh.Q_LEN)
+        zbytes = self.z0.numel() * 4
+        self.R = int(max(1, min(n_steps, Z_BUDGET // zbytes)))
+        self.zs = [torch.empty_like(self.z0) for _ in range(self.R)]
+        nb = sh.n_blocks
+        self.out = torch.empty_like(self.qs[sh.steps[0]])
+        self.lse = torch.empty((sh.B, sh.H, sh.Q_LEN), device=dev, dtype=torch.float32)
+        self.dq = torch.empty(self.out.shape, device=dev, dtype=torch.float32)
+        self.dk = [torch.empty(self.Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(nb)]
+        self.dv = [torch.empty(self.Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(nb)]
+        self.ws = torch.empty(ops.stt_attn_bwd_workspace_size(sh.B, sh.H, sh.H_kv, sh.D, sh.Q_LEN,
+                                                              nb - 1), device=dev, dtype=torch.uint8)
+        self.ce_ws = torch.empty(ops.soft_ce_workspace_size(sc.N, sc.V), device=dev, dtype=torch.uint8)
+        self.loss = torch.empty(1, device=dev, dtype=torch.float32)
+        self.row_loss = torch.empty(sc.N, device=dev, dtype=torch.float32)
+        self.launches_per_step = len(sh.steps) * 3 + 2  # fwd, prep, causal; soft-CE row + loss sum
+
+    def refill(self):
+        for z in self.zs:
+            z.copy_(self.z0)
+
+    def step(self, i, stream, ev=None):
+        sh, ops = self.sh, self.ops
+        for k in sh.steps:
+            if ev is not None:
+                ev["a0"][k].record(stream)
+            ops.stt_attn_fwd(self.qs[k], self.Ks[: k + 1], self.Vs[: k + 1], self.T, sh.scale,
+                             out=self.out, lse=self.lse, stream=stream)
+            ops.stt_attn_bwd(self.qs[k], self.Ks[: k + 1], self.Vs[: k + 1], self.T, self.out,
+                             self.dOs[k], self.lse, sh.scale, dq=self.dq,
+                             dk_blocks=self.dk[: k + 1], dv_blocks=self.dv[: k + 1],
+                             workspace=self.ws, stream=stream)
+            if ev is not None:
+                ev["a1"][k].record(stream)
+        if ev is not None:
+            ev["c0"].record(stream)
+        ops.soft_ce_fwd_bwd_inplace(self.zs[i], self.p, self.g, row_loss=self.row_loss,
+                                    loss=self.loss, workspace=self.ce_ws, stream=stream)
+        if ev is not None:
+            ev["c1"].record(stream)
+
+    def kernel_work(self):
+        """Algorithmic work per step of each kernel (amount, unit)."""
+        sh, sc, T = self.sh, self.sc, self.T
+        D, H = sh.D, sh.H
+        causal = sum(t * (t + 1) // 2 + (sh.Q_LEN - t) * t for t in T) * H * len(sh.steps)
+        suffix = sum(k * t for t in T for k in sh.steps) * H
+        nq = sh.B * H * sh.Q_LEN
+        nkv = sh.B * sh.H_kv * sh.Q_LEN
+        vq = sum(T) * H          # query rows with suffix keys (q < T)
+        vkv = sum(T) * sh.H_kv
+        prep = 0
+        for k in sh.steps:
+            prep += 2 * nq * D * 2 + 4 * nq + 4 * nq              # O, dO; lse; Delta
+            prep += (vq * D * 2 if k > 0 else 0)                  # q
+            prep += 2 * k * vkv * D * 2                           # K_j, V_j, j >= 1
+            prep += 4 * nq * D + 2 * (k + 1) * nkv * D * 4        # dq init; dK_j, dV_j
+        return {
+            "attn_fwd": (4 * D * (causal + suffix), "TFLOP/s"),
+            "attn_bwd_causal": (10 * D * causal, "TFLOP/s"),
+            "attn_bwd_prep": (prep, "GB/s"),
+            "soft_ce": (metrics.soft_ce_algorithmic_bytes(sc.N, sc.V, self.g), "GB/s"),
+        }
+
+
+def timed_run(wb, steps, warmup, stream, L, _lib, clocks=False):
+    """W warm-up steps, then exactly `steps` timed steps in segments of at most
+    wb.R steps (the logits copies are refilled between segments, outside the
+    timed region).  Returns device-event times and the per-launch profile."""
+    import ctypes
+    sh = wb.sh
+    done = 0
+    while done < warmup:
+        wb.refill()
+        n = min(wb.R, warmup - done)
+        for i in range(n):
+            wb.step(i, stream)
+        done += n
+    torch.cuda.synchronize()
+    evs = [{"a0": {k: torch.cuda.Event(enable_timing=True) for k in sh.steps},
+            "a1": {k: torch.cuda.Event(enable_timing=True) for k in sh.steps},
+            "c0": torch.cuda.Event(enable_timing=True), "c1": torch.cuda.Event(enable_timing=True)}
+           for _ in range(steps)]
+    cap = wb.launches_per_step * steps + 16
+    clk = ClockSampler() if clocks else None
+    if clk:
+        time.sleep(0.1)
+    seg_ms = 0.0
+    _lib.check("stt_profile_start", L.stt_profile_start(cap))
+    done = 0
+    while done < steps:
+        wb.refill()
+        torch.cuda.synchronize()
+        n = min(wb.R, steps - done)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(n):
+            wb.step(i, stream, evs[done + i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        seg_ms += t0.elapsed_time(t1)
+        done += n
+    n_rec = ctypes.c_int(0)
+    ids = (ctypes.c_int * cap)()
+    ms = (ctypes.c_float * cap)()
+    _lib.check("stt_profile_stop", L.stt_profile_stop(ctypes.byref(n_rec), ids, ms, cap))
+    clocks_rec = clk.stop() if clk else None
+    attn_ms = sum(e["a0"][k].elapsed_time(e["a1"][k]) for e in evs for k in sh.steps)
+    ce_ms = sum(e["c0"].elapsed_time(e["c1"]) for e in evs)
+    per = {}
+    for i in range(n_rec.value):
+        per.setdefault(L.stt_kernel_name(int(ids[i])).decode(), []).append(float(ms[i]))
+    return {"total_ms": seg_ms, "attn_ms": attn_ms, "ce_ms": ce_ms, "per": per,
+            "launches": n_rec.value, "clocks": clocks_rec}
+
+
+def kernel_rows(wb, per, steps, pk):
+    rows = {}
+    tot = sum(sum(v) for v in per.values())
+    work = wb.kernel_work()
+    for name, v in per.items():
+        ent = {"launches": len(v), "total_ms": round(sum(v), 4), "share": round(sum(v) / tot, 4)}
+        if name in work:
+            amount, unit = work[name]
+            rate = amount * steps / (sum(v) * 1e-3)
+            ach = rate / (1e12 if unit == "TFLOP/s" else 1e9)
+            peak = pk["bf16"] if unit == "TFLOP/s" else pk["hbm"]
+            ent.update({"achieved": round(ach, 2), "unit": unit, "peak": peak,
+                        "frac": round(ach / peak, 4)})
+        rows[name] = ent
+    return rows
+
+
 def run_ours(a):
+    check_world(a)
     rank, world = dist_init("nccl")
     _, _, local = dist_env()
     torch.cuda.set_device(local)
@@ -186,199 +334,122 @@ def run_ours(a):
         build.build()
     barrier(world)
     L = _lib.lib()
-
-    w = wl.WORKLOADS[a.workload]
-    sh, sc = w.attn, w.soft_ce
-    seed = w.seed + 7919 * rank  # independent problem per rank (weak scaling)
-    T, Ks, Vs, qs, dOs = wl.attn_inputs(sh, dev, seed)
-    z0, p, g = wl.soft_ce_inputs(sc, dev, seed, T=T, Q_LEN=sh.Q_LEN)
-    n_z = a.warmup + a.steps
-    zs = [torch.empty_like(z0) for _ in range(n_z)]
-    for z in zs:
-        z.copy_(z0)
-    nb = sh.n_blocks
-    out = torch.empty_like(qs[sh.steps[0]])
-    lse = torch.empty((sh.B, sh.H, sh.Q_LEN), device=dev, dtype=torch.float32)
-    dq = torch.empty(out.shape, device=dev, dtype=torch.float32)
-    dk = [torch.empty(Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(nb)]
-    dv = [torch.empty(Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(nb)]
-    ws = torch.empty(ops.stt_attn_bwd_workspace_size(sh.B, sh.H, sh.H_kv, sh.D, sh.Q_LEN, nb - 1),
-                     device=dev, dtype=torch.uint8)
-    ce_ws = torch.empty(ops.soft_ce_workspace_size(sc.N, sc.V), device=dev, dtype=torch.uint8)
-    loss = torch.empty(1, device=dev, dtype=torch.float32)
-    row_loss = torch.empty(sc.N, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
-
-    def step(i, ev=None):
-        for k in sh.steps:
-            if ev is not None:
-                ev["a0"][k].record(stream)
-            ops.stt_attn_fwd(qs[k], Ks[: k + 1], Vs[: k + 1], T, sh.scale, out=out, lse=lse,
-                             stream=stream)
-            ops.stt_attn_bwd(qs[k], Ks[: k + 1], Vs[: k + 1], T, out, dOs[k], lse, sh.scale, dq=dq,
-                             dk_blocks=dk[: k + 1], dv_blocks=dv[: k + 1], workspace=ws,
-                             stream=stream)
-            if ev is not None:
-                ev["a1"][k].record(stream)
-        if ev is not None:
-            ev["c0"].record(stream)
-        ops.soft_ce_fwd_bwd_inplace(zs[i], p, g, row_loss=row_loss, loss=loss, workspace=ce_ws,
-                                    stream=stream)
-        if ev is not None:
-            ev["c1"].record(stream)
-
-    for i in range(a.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
-    evs = [{"a0": {k: torch.cuda.Event(enable_timing=True) for k in sh.steps},
-            "a1": {k: torch.cuda.Event(enable_timing=True) for k in sh.steps},
-            "c0": torch.cuda.Event(enable_timing=True), "c1": torch.cuda.Event(enable_timing=True)}
-           for _ in range(a.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches_per_step = len(sh.steps) * 3 + 2  # fwd, bwd prep, bwd causal; soft-CE + loss sum
-    cap = launches_per_step * a.steps + 16
-    clk = ClockSampler() if rank == 0 else None
-    time.sleep(0.1 if clk else 0)
-    barrier(world)
-    torch.cuda.synchronize()
-    _lib.check("stt_profile_start", L.stt_profile_start(cap))
-    t0.record(stream)
-    for i in range(a.steps):
-        step(a.warmup + i, evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    import ctypes
-    n = ctypes.c_int(0)
-    ids = (ctypes.c_int * cap)()
-    ms = (ctypes.c_float * cap)()
-    _lib.check("stt_profile_stop", L.stt_profile_stop(ctypes.byref(n), ids, ms, cap))
-    clocks = clk.stop() if clk else None
-    assert ops.stt_device_error(stream) == 0
-
-    total_ms = allreduce_max(t0.elapsed_time(t1), world, dev)
-    attn_ms = sum(e["a0"][k].elapsed_time(e["a1"][k]) for e in evs for k in sh.steps)
-    ce_ms = sum(e["c0"].elapsed_time(e["c1"]) for e in evs)
-    attn_ms_max = allreduce_max(attn_ms, world, dev)
-    ce_ms_max = allreduce_max(ce_ms, world, dev)
-
-    ff, fb = metrics.attn_useful_flops(sh, T)
-    flops_all = allreduce_sum(float(ff + fb) * a.steps, world, dev)
-    ce_bytes = metrics.soft_ce_algorithmic_bytes(sc.N, sc.V, g)
-    ce_bytes_all = allreduce_sum(float(ce_bytes) * a.steps, world, dev)
-    value = flops_all / (attn_ms_max * 1e-3) / 1e12
-    ce_gbs = ce_bytes_all / (ce_ms_max * 1e-3) / 1e9
-
-    # per-kernel shares and the roofline of the dominant kernel
-    per = {}
-    for i in range(n.value):
-        per.setdefault(int(ids[i]), []).append(float(ms[i]))
     pk = peaks()
-    kinfo = kernel_algorithmic(sh, sc, T, g)
-    kern_rows = {}
-    tot_k = sum(sum(v) for v in per.values())
-    for kid, v in per.items():
-        name = L.stt_kernel_name(kid).decode()
-        units = kinfo.get(name)
-        ent = {"launches": len(v), "total_ms": round(sum(v), 4), "share": round(sum(v) / tot_k, 4)}
-        if units:
-            amount, unit = units
-            rate = amount * a.steps / (sum(v) * 1e-3)
-            ent["achieved"] = round(rate / (1e12 if unit == "TFLOP/s" else 1e9), 2)
-            ent["unit"] = unit
-        kern_rows[name] = ent
-    dom_id = max(per, key=lambda kk: sum(per[kk]))
-    dom = L.stt_kernel_name(dom_id).decode()
-    src, bound = KERNELS[dom_id]
-    if bound == "tensor":
-        peak, unit = pk["bf16_sustained"], "TFLOP/s"
-    else:
-        peak, unit = pk["hbm"], "GB/s"
-    achieved = kern_rows[dom].get("achieved")
-    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4) if achieved else None,
-                "traffic": traffic_for(dom, src, a.workload),
-                "peak_src": pk["src"] + (" sustained" if bound == "tensor" else " copy")}
 
-    e2e = (run_e2e(a, sh, sc, T, Ks, Vs, qs, dOs, z0, p, g, ops, dev, stream, ff + fb, world)
-           if a.e2e_steps > 0 else None)
+    name = a.workload
+    seed = wl.WORKLOADS[name].seed + 7919 * rank  # an independent problem per rank (weak scaling)
+    wb = Workbench(name, dev, seed, a.warmup + a.steps)
+    T = wb.T
+    launches = wb.launches_per_step * a.steps
+    barrier(world)
+    torch.cuda.synchronize()
+    r = timed_run(wb, a.steps, a.warmup, stream, L, _lib, clocks=(rank == 0))
+    barrier(world)
+    assert ops.stt_device_error(stream) == 0
+    sh, sc = wb.sh, wb.sc
+
+    total_ms = allreduce(r["total_ms"], world, dev, "max")
+    attn_ms = allreduce(r["attn_ms"], world, dev, "max")
+    ce_ms = allreduce(r["ce_ms"], world, dev, "max")
+    ff, fb = metrics.attn_useful_flops(sh, wb.T)
+    flops_all = allreduce(float(ff + fb) * a.steps, world, dev, "sum")
+    ce_bytes = metrics.soft_ce_algorithmic_bytes(sc.N, sc.V, wb.g)
+    ce_all = allreduce(float(ce_bytes) * a.steps, world, dev, "sum")
+    value = flops_all / (attn_ms * 1e-3) / 1e12
+    ce_gbs = ce_all / (ce_ms * 1e-3) / 1e9
+
+    krows = kernel_rows(wb, r["per"], a.steps, pk)
+    dom = max(r["per"], key=lambda kk: sum(r["per"][kk]))
+    bound = KERNELS[dom][1]
+    d = krows[dom]
+    roofline = {"kernel": dom, "bound": bound, "achieved": d.get("achieved"), "peak": d.get("peak"),
+                "unit": d.get("unit"), "frac": d.get("frac"), "traffic": traffic_for(dom, name),
+                "peak_src": pk["src"] + (" bf16 dense burst (kernel timed alone, seconds-short "
+                                         "timed region at max SM clock)" if bound == "tensor"
+                                         else " HBM copy bandwidth")}
+
+    e2e = (run_e2e(a, wb, dev, stream, ff + fb, world) if a.e2e_steps > 0 else None)
+
+    others = {}
+    if not a.no_other_workloads:
+        del wb
+        torch.cuda.empty_cache()
+        for on in ("llama8b", "varlen", "llama70b", "long_ttt"):
+            if on == name:
+                continue
+            ob = Workbench(on, dev, wl.WORKLOADS[on].seed + 7919 * rank, 3 + a.other_steps)
+            ro = timed_run(ob, a.other_steps, 3, stream, L, _lib)
+            assert ops.stt_device_error(stream) == 0
+            off, ofb = metrics.attn_useful_flops(ob.sh, ob.T)
+            o_attn = allreduce(ro["attn_ms"], world, dev, "max")
+            o_ce = allreduce(ro["ce_ms"], world, dev, "max")
+            o_fl = allreduce(float(off + ofb) * a.other_steps, world, dev, "sum")
+            o_cb = allreduce(float(metrics.soft_ce_algorithmic_bytes(ob.sc.N, ob.sc.V, ob.g))
+                             * a.other_steps, world, dev, "sum")
+            kr = kernel_rows(ob, ro["per"], a.other_steps, pk)
+            others[on] = {"steps": a.other_steps, "warmup": 3,
+                          "attn_tflops": round(o_fl / (o_attn * 1e-3) / 1e12, 2),
+                          "attn_frac_of_bf16_burst": round(o_fl / (o_attn * 1e-3) / 1e12 / pk["bf16"], 4),
+                          "soft_ce_gbs": round(o_cb / (o_ce * 1e-3) / 1e9, 1),
+                          "kernels": {kn: {x: kv[x] for x in ("achieved", "unit", "frac", "share")
+                                           if x in kv} for kn, kv in kr.items()}}
+            del ob
+            torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(total_ms / a.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": a.workload, "B": sh.B, "H": sh.H, "H_kv": sh.H_kv, "D": sh.D,
-                   "Q_LEN": sh.Q_LEN, "T": T if len(T) <= 16 else f"{len(T)} values",
-                   "ttt_steps": list(sh.steps), "soft_ce_N": sc.N, "soft_ce_V": sc.V,
-                   "parallelism": f"replicas x{world}",
+        "config": {"workload": name, "B": sh.B, "H": sh.H, "H_kv": sh.H_kv, "D": sh.D,
+                   "Q_LEN": sh.Q_LEN, "T": T if len(T) <= 16 else f"{len(T)} values in [{min(T)}, {max(T)}]", "ttt_steps": list(sh.steps),
+                   "soft_ce_N": sc.N, "soft_ce_V": sc.V, "parallelism": f"replicas x{world}",
                    "l2": "inputs > L2: each step streams a fresh logits copy (> 129 MB) "
                          "through the soft-CE, flushing L2 between steps"},
+        "attn_frac_of_bf16_burst": round(value / pk["bf16"], 4),
         "soft_ce": {"metric": "in-place soft-CE algorithmic GB/s", "value": round(ce_gbs, 1),
                     "unit": "GB/s", "frac_of_measured_hbm": round(ce_gbs / pk["hbm"], 4),
-                    "ms_per_step": round(ce_ms_max / a.steps, 4)},
-        "attn_ms_per_step": round(attn_ms_max / a.steps, 4),
+                    "ms_per_step": round(ce_ms / a.steps, 4)},
+        "attn_ms_per_step": round(attn_ms / a.steps, 4),
         "roofline": roofline,
-        "kernels": kern_rows,
+        "kernels": krows,
         # every launch of the library's kernels in the timed region (the profiler
         # records the soft-CE row kernel and its loss sum as one unit)
-        "gpu_launches": launches_per_step * a.steps,
+        "gpu_launches": launches,
+        "gpu_launches_recorded": r["launches"],
         "e2e": e2e,
-        "clocks": clocks,
+        "clocks": r["clocks"],
+        "other_workloads": others or None,
     }
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(a.workload, samples=1)
+        line["cpu_baseline"] = cpu_baseline(name)
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
 
 
-def kernel_algorithmic(sh, sc, T, g):
-    """Algorithmic work per step of each kernel (amount, unit)."""
-    D, H = sh.D, sh.H
-    causal = sum(t * (t + 1) // 2 + (sh.Q_LEN - t) * t for t in T) * H * len(sh.steps)
-    suffix = sum(k * t for t in T for k in sh.steps) * H
-    bpe = 2
-    nq = sh.B * H * sh.Q_LEN
-    nkv = sh.B * sh.H_kv * sh.Q_LEN
-    # rows with suffix keys (q < T): only they need q, K_j and V_j, j >= 1
-    vq = sum(T) * H
-    vkv = sum(T) * sh.H_kv
-    prep_bytes = 0
-    for k in sh.steps:
-        prep_bytes += 2 * nq * D * bpe + 4 * nq + 4 * nq             # O, dO; lse; Delta
-        prep_bytes += (vq * D * bpe if k > 0 else 0)                 # q
-        prep_bytes += 2 * k * vkv * D * bpe                          # K_j, V_j, j >= 1
-        prep_bytes += 4 * nq * D + 2 * (k + 1) * nkv * D * 4         # dq init; dK_j, dV_j
-    return {
-        "attn_fwd": (4 * D * (causal + suffix), "TFLOP/s"),
-        "attn_bwd_causal": (10 * D * causal, "TFLOP/s"),
-        "attn_bwd_prep": (prep_bytes, "GB/s"),
-        "soft_ce": (metrics.soft_ce_algorithmic_bytes(sc.N, sc.V, g), "GB/s"),
-    }
-
-
-def run_e2e(a, sh, sc, T, Ks, Vs, qs, dOs, z0, p, g, ops, dev, stream, flops, world):
+def run_e2e(a, wb, dev, stream, flops, world):
     """The same metric through the public API with HOST buffers: every step copies
     its inputs from pinned host memory and reads its results back."""
+    ops, sh = wb.ops, wb.sh
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
-    hK = [pin(x) for x in Ks]
-    hV = [pin(x) for x in Vs]
-    hq = {k: pin(qs[k]) for k in sh.steps}
-    hd = {k: pin(dOs[k]) for k in sh.steps}
-    hz, hp, hg = pin(z0), pin(p), pin(g)
+    hK = [pin(x) for x in wb.Ks]
+    hV = [pin(x) for x in wb.Vs]
+    hq = {k: pin(wb.qs[k]) for k in sh.steps}
+    hd = {k: pin(wb.dOs[k]) for k in sh.steps}
+    hz, hp, hg = pin(wb.z0), pin(wb.p), pin(wb.g)
     nb = sh.n_blocks
-    dK = [torch.empty_like(x) for x in Ks]
-    dV = [torch.empty_like(x) for x in Vs]
-    dq_ = {k: torch.empty_like(qs[k]) for k in sh.steps}
-    ddo = {k: torch.empty_like(dOs[k]) for k in sh.steps}
-    dz, dp_, dg = torch.empty_like(z0), torch.empty_like(p), torch.empty_like(g)
-    o_h = torch.empty(qs[sh.steps[0]].shape, dtype=torch.bfloat16).pin_memory()
+    dK = [torch.empty_like(x) for x in wb.Ks]
+    dV = [torch.empty_like(x) for x in wb.Vs]
+    dq_ = {k: torch.empty_like(wb.qs[k]) for k in sh.steps}
+    ddo = {k: torch.empty_like(wb.dOs[k]) for k in sh.steps}
+    dz, dp_, dg = torch.empty_like(wb.z0), torch.empty_like(wb.p), torch.empty_like(wb.g)
+    o_h = torch.empty(wb.out.shape, dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty((sh.B, sh.H, sh.Q_LEN), dtype=torch.float32).pin_memory()
-    dq_h = torch.empty(qs[sh.steps[0]].shape, dtype=torch.float32).pin_memory()
-    dkv_h = [torch.empty(Ks[0].shape, dtype=torch.float32).pin_memory() for _ in range(2 * nb)]
-    z_h = torch.empty(z0.shape, dtype=torch.float32).pin_memory()
+    dq_h = torch.empty(wb.out.shape, dtype=torch.float32).pin_memory()
+    dkv_h = [torch.empty(wb.Ks[0].shape, dtype=torch.float32).pin_memory() for _ in range(2 * nb)]
+    z_h = torch.empty(wb.z0.shape, dtype=torch.float32).pin_memory()
     loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in hK + hV + list(hq.values()) + list(hd.values()))
     h2d += sum(x.numel() * x.element_size() for x in (hz, hp, hg))
@@ -398,8 +469,8 @@ def run_e2e(a, sh, sc, T, Ks, Vs, qs, dOs, z0, p, g, ops, dev, stream, flops, wo
         dp_.copy_(hp, non_blocking=True)
         dg.copy_(hg, non_blocking=True)
         for k in sh.steps:
-            o, l = ops.stt_attn_fwd(dq_[k], dK[: k + 1], dV[: k + 1], T, sh.scale, stream=stream)
-            gq, gk, gv = ops.stt_attn_bwd(dq_[k], dK[: k + 1], dV[: k + 1], T, o, ddo[k], l,
+            o, l = ops.stt_attn_fwd(dq_[k], dK[: k + 1], dV[: k + 1], wb.T, sh.scale, stream=stream)
+            gq, gk, gv = ops.stt_attn_bwd(dq_[k], dK[: k + 1], dV[: k + 1], wb.T, o, ddo[k], l,
                                           sh.scale, stream=stream)
             o_h.copy_(o, non_blocking=True)
             lse_h.copy_(l, non_blocking=True)
@@ -421,54 +492,109 @@ def run_e2e(a, sh, sc, T, Ks, Vs, qs, dOs, z0, p, g, ops, dev, stream, flops, wo
         one()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_ = allreduce_max(e0.elapsed_time(e1), world, dev)
-    tot = allreduce_sum(float(flops) * a.e2e_steps, world, dev)
+    ms_ = allreduce(e0.elapsed_time(e1), world, dev, "max")
+    tot = allreduce(float(flops) * a.e2e_steps, world, dev, "sum")
     return {"value": round(tot / (ms_ * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms_ / a.e2e_steps, 3), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
 
 
 # ------------------------------------------------------ oracle on the CPU --
-def cpu_baseline(workload, samples=1):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload: one
-    query head (b=0, h=0) at the last TTT step, forward and backward, plus the
-    soft-CE on 256 rows.  Returns the attention useful TFLOP/s of the sample."""
+def _oracle_head_task(workload, b, h, k):
+    """Oracle forward + backward of one query head at TTT step k (inputs drawn
+    with the workload's CPU generator); returns the seconds the oracle took."""
     import oracle
+    w = wl.WORKLOADS[workload]
+    sh = w.attn
+    T = wl.draw_T(sh, w.seed)
+    g = h // (sh.H // sh.H_kv)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    Kb = [f(wl.kv_block(sh, "K", j, "cpu", w.seed)[b, g]) for j in range(k + 1)]
+    Vb = [f(wl.kv_block(sh, "V", j, "cpu", w.seed)[b, g]) for j in range(k + 1)]
+    q = f(wl.step_query(sh, k, "cpu", w.seed)[b, h])
+    dO = f(wl.step_dout(sh, k, "cpu", w.seed)[b, h])
+    t0 = time.perf_counter()
+    O, l = oracle.attention.head_forward_keyset(q, Kb, Vb, T[b], sh.scale)
+    oracle.attention.head_backward_keyset(q, Kb, Vb, T[b], sh.scale, dO, O, l)
+    return time.perf_counter() - t0
+
+
+def _pool_units(workload, n):
+    """The first n units of the sampled plan: batch 0, KV group 0 with all its
+    query heads, TTT steps spread from the last to the first."""
+    sh = wl.WORKLOADS[workload].attn
+    G = sh.H // sh.H_kv
+    ks = sorted(sh.steps, reverse=True)
+    n_steps = max(1, n // G)
+    pick = [ks[round(i * (len(ks) - 1) / max(1, n_steps - 1))] for i in range(n_steps)] \
+        if n_steps > 1 else [ks[0]]
+    return [(0, h, k) for k in dict.fromkeys(pick) for h in range(G)]
+
+
+def cpu_baseline(workload, mode="pool"):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload.
+
+    mode "pool": one wave of concurrent single-threaded oracle tasks, one per
+    host core, over the sampled units (batch 0, KV group 0 with all its query
+    heads, TTT steps spread over 0..K-1); value = their useful FLOPs / wall
+    time of the wave.  mode "one": one query head (b=0, h=0) at the last TTT
+    step in this process, NumPy BLAS at its default thread count.
+    Plus the soft-CE oracle on 256 rows."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
     w = wl.WORKLOADS[workload]
     sh, sc = w.attn, w.soft_ce
     T = wl.draw_T(sh, w.seed)
-    k = sh.steps[-1]
-    Kb = [wl.kv_block(sh, "K", j, "cpu", w.seed)[0, 0].float().numpy().astype(np.float64)
-          for j in range(k + 1)]
-    Vb = [wl.kv_block(sh, "V", j, "cpu", w.seed)[0, 0].float().numpy().astype(np.float64)
-          for j in range(k + 1)]
-    q = wl.step_query(sh, k, "cpu", w.seed)[0, 0].float().numpy().astype(np.float64)
-    dO = wl.step_dout(sh, k, "cpu", w.seed)[0, 0].float().numpy().astype(np.float64)
-    ent = metrics.useful_entries(T[0], sh.Q_LEN, k)
-    flops = 14 * sh.D * ent
-    t_attn = 0.0
-    for _ in range(samples):
+    cores = os.cpu_count() or 1
+    if mode == "pool":
+        units = _pool_units(workload, cores)
+        saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
+        for v in saved:
+            os.environ[v] = "1"
+        try:
+            with cf.ProcessPoolExecutor(max_workers=len(units),
+                                        mp_context=mp.get_context("spawn")) as ex:
+                t0 = time.perf_counter()
+                secs = list(ex.map(_oracle_head_task, *zip(*[(workload,) + u for u in units])))
+                wall_all = time.perf_counter() - t0
+        finally:
+            for v, val in saved.items():
+                if val is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = val
+        used = len(units)
+        wall = max(secs)  # the tasks run concurrently, one per core
+        sample = (f"{workload}: {len(units)} concurrent single-threaded oracle tasks (fwd+bwd of one "
+                  f"query head each: b=0, KV group 0, heads 0..{sh.H // sh.H_kv - 1}, TTT steps "
+                  f"{sorted({u[2] for u in units})}); oracle time of the slowest task {wall:.1f} s "
+                  f"(wave wall time with worker start-up and input generation {wall_all:.1f} s)")
+    else:
+        units = [(0, 0, sh.steps[-1])]
         t0 = time.perf_counter()
-        O, l = oracle.attention.head_forward_keyset(q, Kb, Vb, T[0], sh.scale)
-        oracle.attention.head_backward_keyset(q, Kb, Vb, T[0], sh.scale, dO, O, l)
-        t_attn += time.perf_counter() - t0
+        _oracle_head_task(workload, *units[0])
+        wall = time.perf_counter() - t0
+        used = cores
+        sample = (f"{workload}: one query head (b=0, h=0) at TTT step k={sh.steps[-1]}, fwd+bwd, "
+                  f"NumPy BLAS at its default thread count, {wall:.1f} s")
+    flops = sum(14 * sh.D * metrics.useful_entries(T[b], sh.Q_LEN, k) for b, _, k in units)
+    full = metrics.attn_useful_flops(sh, T)
     rows = 256
     g0 = torch.Generator().manual_seed(w.seed)
     z = (torch.randn((rows, sc.V), generator=g0) * sc.z_std).numpy()
     lg = torch.randn((rows, sc.V), generator=g0) * sc.p_std
     pp = torch.softmax(lg / sc.p_temp, dim=1).numpy()
     gg = np.full(rows, 1.0 / sc.N, dtype=np.float32)
+    import oracle
     t0 = time.perf_counter()
     oracle.soft_ce.soft_ce(z, pp, gg)
     t_ce = time.perf_counter() - t0
-    return {"value": round(flops * samples / t_attn / 1e12, 6), "unit": "TFLOP/s",
-            "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{workload}: query head (b=0,h=0) at TTT step k={k}, T={T[0]}, fwd+bwd in fp64 "
-                      f"({t_attn / samples:.2f} s); soft-CE oracle on {rows} rows of V={sc.V} "
-                      f"({t_ce:.2f} s)",
+    value = flops / wall / 1e12
+    return {"value": round(value, 6), "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+            "sample": sample + f"; soft-CE oracle on {rows} rows of V={sc.V} ({t_ce:.2f} s)",
+            "full_config_s_extrapolated": round(sum(full) / (value * 1e12), 1),
             "soft_ce_gbs": round(12 * rows * sc.V / t_ce / 1e9, 4),
-            "threads_note": "NumPy BLAS at its default thread count (all cores); element-wise "
-                            "steps single-threaded"}
+            "host_cores": cores}
 
 
 def run_reference(a):
@@ -481,7 +607,7 @@ def run_reference(a):
     cb = None
     for i in range(a.warmup + a.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(a.workload, samples=1)
+        cb = cpu_baseline(a.workload, mode="one")
         if i >= a.warmup:
             times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)

@@ -78,10 +78,36 @@ STT_API int stt_version(void);
 /*
  * Reads and clears the device-side error word (bitwise OR of the STT_DEVERR_*
  * sites whose bounded wait ran out since the last call).  Synchronises
- * `stream` first.  Returns STT_OK and stores the word in *word, or
- * STT_ERR_CUDA.
+ * `stream` first, then stores the word in *word and returns STT_ERR_TIMEOUT
+ * if any STT_DEVERR_*_WAIT bit is set, STT_OK otherwise (the word is stored
+ * in both cases), or STT_ERR_CUDA if the synchronisation or a read failed.
  */
 STT_API int stt_device_error(void* stream, uint32_t* word);
+
+/*
+ * Failure-detection test hooks (no counterpart on the pages).  Every wait of
+ * the kernels on an mbarrier is bounded by a wall-clock budget (2 s by
+ * default); when it runs out, the waiting thread records its site in the
+ * device error word and gives up, the other roles of the CTA give up in turn,
+ * and the kernel returns (its outputs are then undefined).
+ *
+ * stt_debug_set_wait_budget(ns) sets that budget, in nanoseconds, on the
+ * current device for every kernel of the library launched afterwards; 0
+ * restores the default.  Returns STT_OK or STT_ERR_CUDA.
+ *
+ * stt_debug_inject(what) makes every later launch of the named kernels skip
+ * one step on purpose, so that a bounded wait runs out without any fault:
+ *   STT_INJECT_FWD_WITHHOLD_Q  the attention forward's producer never loads
+ *                              the query tile, so the wait for it runs out;
+ *                              every copy already issued is waited for before
+ *                              the CTA exits, and no tensor-core product is
+ *                              issued.
+ * 0 switches injection off.  Unknown bits return STT_ERR_INVALID_ARG.  The
+ * setting is process-wide; it is meant for tests, never for production runs.
+ */
+STT_API int stt_debug_set_wait_budget(uint64_t ns);
+STT_API int stt_debug_inject(uint32_t what);
+#define STT_INJECT_FWD_WITHHOLD_Q 0x1u
 
 /* --------------------------------------------------------------------------
  * Sparse-tree attention, forward.
@@ -172,13 +198,17 @@ STT_API int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, in
  *  z, p, g, N, V, row_loss, loss: as soft_ce_fwd_bwd_inplace.
  *  N must be <= 65536 rows (the scratch size); larger N returns
  *  STT_ERR_WORKSPACE without launching anything.
- *  The first call on a device looks up the scratch array's device address
- *  (cudaGetSymbolAddress, with that device current) and caches it; make that
- *  first call before any stream capture.  All calls share the one array, so
- *  calls whose kernels overlap on the GPU (different streams, or threads
- *  without ordering) race on it and must be serialised by the caller.  Every
- *  scratch entry a call reads is written earlier in the same call, so the
- *  previous call's leftovers never affect the result.
+ *  Every call looks up the scratch array's device address on the current
+ *  device (cudaGetSymbolAddress), so the address stays right after a
+ *  cudaDeviceReset or a new primary context; the first call on a device also
+ *  loads the library's kernels there, so make that first call before any
+ *  stream capture.  All calls share the one array, so calls whose kernels
+ *  overlap on the GPU (different streams, or threads without ordering) race
+ *  on it and must be serialised by the caller.  Every scratch entry a call
+ *  reads is written earlier in the same call, so the previous call's
+ *  leftovers never affect the result.  Status codes are those of
+ *  soft_ce_fwd_bwd_inplace (a CUDA failure the device does not support is
+ *  STT_ERR_UNSUPPORTED, any other STT_ERR_CUDA).
  * ------------------------------------------------------------------------ */
 STT_API int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const float* g, int64_t N,
                                             int64_t V, float* row_loss, float* loss,
@@ -215,6 +245,7 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_DEVERR_BWD_WAIT 0x2u
 #define STT_DEVERR_CE_WAIT 0x4u
 #define STT_DEVERR_SMEM_ALIGN 0x8u
+#define STT_DEVERR_WAIT_MASK (STT_DEVERR_FWD_WAIT | STT_DEVERR_BWD_WAIT | STT_DEVERR_CE_WAIT)
 
 #ifdef __cplusplus
 }

@@ -28,6 +28,8 @@ EXPORTS = (
     "stt_status_string",
     "stt_version",
     "stt_device_error",
+    "stt_debug_set_wait_budget",
+    "stt_debug_inject",
     "stt_attn_fwd",
     "stt_attn_bwd_workspace_size",
     "stt_attn_bwd",
@@ -58,6 +60,10 @@ def _declare(L):
     L.stt_version.restype = i32
     L.stt_device_error.argtypes = [vp, c.POINTER(c.c_uint32)]
     L.stt_device_error.restype = i32
+    L.stt_debug_set_wait_budget.argtypes = [c.c_uint64]
+    L.stt_debug_set_wait_budget.restype = i32
+    L.stt_debug_inject.argtypes = [c.c_uint32]
+    L.stt_debug_inject.restype = i32
     L.stt_attn_fwd.argtypes = [vp, c.POINTER(vp), c.POINTER(vp), c.POINTER(c.c_int32),
                                i32, i32, i32, i32, i32, i32, f32, vp, vp, vp]
     L.stt_attn_fwd.restype = i32

@@ -894,5 +894,6 @@ cudaError_t attn_bwd_launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_
 }
 
 STT_DEFINE_ERROR_ACCESSOR(attn_bwd_error_word)
+STT_DEFINE_BUDGET_SETTER(attn_bwd_set_wait_budget)
 
 }  // namespace stt

@@ -57,6 +57,7 @@ struct FwdParams {
   float* lse;
   int B, H, H_kv, Q_LEN, k, n_qt, G;
   float scale_log2;
+  uint32_t inject;  // STT_INJECT_* test hooks (0 in normal use)
   int T[kMaxBatch];
 };
 
@@ -179,7 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane < 2 && n_kv > 0) {
       const bool is_k = lane == 0;
       const int bhk = b * P.H_kv + hk;
-      if (is_k) {
+      // Test hook: the query tile is never loaded, so the S issuer's wait for
+      // it runs out and every role of the CTA gives up in turn.
+      const bool withhold_q = (P.inject & STT_INJECT_FWD_WITHHOLD_Q) != 0;
+      if (is_k && !withhold_q) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         mbar_arrive_expect_tx(&bar_q, L::kQ);
@@ -234,9 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &bar_sfx_full[st], cb * kColBlock, q0, bhk);
         ++issued_s;
       }
-      if (!ok) {
-        // Gave up: let every copy this lane issued land before the CTA exits.
-        if (is_k) mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
+      if (!ok || withhold_q) {
+        // Gave up (or nothing will consume the copies): let every copy this
+        // lane issued land before the CTA exits.
+        if (is_k && !withhold_q) mbar_wait(&bar_q, 0, STT_DEVERR_FWD_WAIT);
         for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
           mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u, STT_DEVERR_FWD_WAIT);
         for (int i = (issued_s > kStages ? issued_s - kStages : 0); i < issued_s; ++i)
@@ -582,6 +587,7 @@ cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   P.n_qt = (a.Q_LEN + kTile - 1) / kTile;
   P.G = a.H / a.H_kv;
   P.scale_log2 = a.scale * kLog2e;
+  P.inject = debug_inject();
   for (int b = 0; b < a.B; ++b) P.T[b] = a.T[b];
   const int smem = FwdSmem<D>::alloc;
   e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -602,5 +608,6 @@ cudaError_t attn_fwd_launch(const AttnArgs& a, void* out, float* lse, cudaStream
 }
 
 STT_DEFINE_ERROR_ACCESSOR(attn_fwd_error_word)
+STT_DEFINE_BUDGET_SETTER(attn_fwd_set_wait_budget)
 
 }  // namespace stt

@@ -54,6 +54,22 @@ cudaError_t attn_bwd_launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_
 cudaError_t soft_ce_error_word(uint32_t* w);
 cudaError_t attn_fwd_error_word(uint32_t* w);
 cudaError_t attn_bwd_error_word(uint32_t* w);
+// Per-file bounded-wait budgets (nanoseconds; 0 restores the default).
+cudaError_t soft_ce_set_wait_budget(uint64_t ns);
+cudaError_t attn_fwd_set_wait_budget(uint64_t ns);
+cudaError_t attn_bwd_set_wait_budget(uint64_t ns);
+
+// Test hooks set by stt_debug_inject (STT_INJECT_* bits), read at launch.
+uint32_t debug_inject();
+
+// Status code of a CUDA error: cudaErrorNotSupported (an unsupported device
+// or driver feature) is STT_ERR_UNSUPPORTED (-2), every other failure
+// STT_ERR_CUDA (-4).
+inline int status_from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return 0;
+  if (e == cudaErrorNotSupported) return -2;
+  return -4;
+}
 
 // Per-launch timing hooks (profile.cu); no-ops unless stt_profile_start ran.
 void prof_before(cudaStream_t s, int kernel_id);

@@ -27,8 +27,20 @@ static __device__ uint32_t g_device_error = 0;
   }
 
 // Wall-clock budget of one bounded wait: far longer than any legitimate wait
-// inside these kernels (each runs for milliseconds).
+// inside these kernels (each runs for milliseconds).  A device variable of
+// this translation unit, so that the host can shorten it (tests make a wait
+// run out on purpose and want the kernel back quickly); see
+// STT_DEFINE_BUDGET_SETTER.
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;  // 2 s
+static __device__ uint64_t g_wait_budget_ns = kWaitBudgetNs;
+
+// Sets this translation unit's wait budget on the current device (0 restores
+// the default).
+#define STT_DEFINE_BUDGET_SETTER(fn)                                               \
+  cudaError_t fn(uint64_t ns) {                                                    \
+    const uint64_t v = ns ? ns : kWaitBudgetNs;                                    \
+    return cudaMemcpyToSymbol(g_wait_budget_ns, &v, sizeof(uint64_t));             \
+  }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -92,9 +104,10 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t budget = *(volatile uint64_t*)&g_wait_budget_ns;
   while (true) {
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+    if (globaltimer_ns() - t0 > budget) {
       record_error(site);
       return false;
     }
@@ -128,9 +141,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t site) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t budget = *(volatile uint64_t*)&g_wait_budget_ns;
   while (true) {
     if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+    if (globaltimer_ns() - t0 > budget) {
       record_error(site);
       return false;
     }

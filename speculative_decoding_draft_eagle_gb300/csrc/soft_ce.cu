@@ -815,6 +815,7 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
 }
 
 STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)
+STT_DEFINE_BUDGET_SETTER(soft_ce_set_wait_budget)
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the in-place soft-CE.
@@ -824,30 +825,21 @@ STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)
 // Every GPU that loads the library holds this array (256 KB) until the
 // process exits.  In host code `g_noalloc_scratch` is only a host-side stand-in
 // for the symbol, not a device address, so the device address is looked up
-// once per device with cudaGetSymbolAddress (with that device current) and
-// cached; kernels are always handed that looked-up pointer.
+// with cudaGetSymbolAddress on the current device at every call (a cached
+// address would go stale after cudaDeviceReset or a new primary context);
+// kernels are always handed that looked-up pointer.
 namespace {
 
 constexpr int64_t kNoAllocMaxRows = 65536;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocMaxRows];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on first use).
+// Device address of the scratch array on the current device.
 int noalloc_scratch(float** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return STT_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return STT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return STT_ERR_CUDA;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  if (p == nullptr) return STT_ERR_CUDA;
+  *out = static_cast<float*>(p);
   return STT_OK;
 }
 
@@ -873,7 +865,7 @@ extern "C" int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const f
     if (N * (int64_t)plan.C > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
     const cudaError_t e = stt::soft_ce_launch(plan, z, p, g, N, V, row_loss, loss, scratch,
                                               static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? STT_OK : STT_ERR_CUDA;
+    return stt::status_from_cuda(e);
   } catch (...) {
     return STT_ERR_CUDA;
   }

@@ -2,6 +2,7 @@
 // status codes, and dispatch to the kernel launchers.  No entry point
 // allocates device memory or synchronises (except stt_device_error, which is
 // documented to synchronise its stream).
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -25,17 +26,21 @@ void* tensor_map_encoder() {
   return fn;
 }
 
+namespace {
+std::atomic<uint32_t> g_inject{0};
+}  // namespace
+
+uint32_t debug_inject() { return g_inject.load(std::memory_order_relaxed); }
+
 }  // namespace stt
 
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return STT_OK;
-  if (e == cudaErrorNotSupported) return STT_ERR_UNSUPPORTED;
-  return STT_ERR_CUDA;
-}
+int from_cuda(cudaError_t e) { return stt::status_from_cuda(e); }
+
+static_assert(STT_ERR_UNSUPPORTED == -2 && STT_ERR_CUDA == -4, "status_from_cuda codes");
 
 // Shared validation of the attention arguments; fills `a` on success.
 int check_attn(const void* q, const void* const* k_blocks, const void* const* v_blocks,
@@ -104,6 +109,19 @@ int stt_device_error(void* stream, uint32_t* word) {
   if (stt::attn_bwd_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
   w |= part;
   *word = w;
+  return (w & STT_DEVERR_WAIT_MASK) ? STT_ERR_TIMEOUT : STT_OK;
+}
+
+int stt_debug_set_wait_budget(uint64_t ns) {
+  cudaError_t e = stt::soft_ce_set_wait_budget(ns);
+  if (e == cudaSuccess) e = stt::attn_fwd_set_wait_budget(ns);
+  if (e == cudaSuccess) e = stt::attn_bwd_set_wait_budget(ns);
+  return from_cuda(e);
+}
+
+int stt_debug_inject(uint32_t what) {
+  if (what & ~(uint32_t)STT_INJECT_FWD_WITHHOLD_Q) return STT_ERR_INVALID_ARG;
+  stt::g_inject.store(what, std::memory_order_relaxed);
   return STT_OK;
 }
 

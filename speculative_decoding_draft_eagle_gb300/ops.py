@@ -23,6 +23,8 @@ __all__ = [
     "soft_ce_fwd_bwd_inplace_noalloc",
     "soft_ce_workspace_size",
     "stt_device_error",
+    "stt_debug_set_wait_budget",
+    "stt_debug_inject",
     "stt_version",
 ]
 
@@ -196,10 +198,28 @@ def soft_ce_fwd_bwd_inplace_noalloc(z: torch.Tensor, p: torch.Tensor, g: torch.T
     return loss, row_loss
 
 
+STT_ERR_TIMEOUT = -5
+
+
 def stt_device_error(stream=None) -> int:
+    """Synchronises the stream, then reads and clears the device error word
+    (0 when no bounded wait ran out).  STT_ERR_TIMEOUT is reported through
+    the returned word's STT_DEVERR_*_WAIT bits, not raised."""
     w = ctypes.c_uint32(0)
-    check("stt_device_error", lib().stt_device_error(_stream(stream), ctypes.byref(w)))
+    st = lib().stt_device_error(_stream(stream), ctypes.byref(w))
+    if st != STT_ERR_TIMEOUT:
+        check("stt_device_error", st)
     return int(w.value)
+
+
+def stt_debug_set_wait_budget(ns: int) -> None:
+    """Bounded-wait budget of every kernel on the current device (0: default)."""
+    check("stt_debug_set_wait_budget", lib().stt_debug_set_wait_budget(int(ns)))
+
+
+def stt_debug_inject(what: int) -> None:
+    """Test hook: STT_INJECT_* bits (0 switches injection off)."""
+    check("stt_debug_inject", lib().stt_debug_inject(int(what)))
 
 
 def stt_version() -> int:

@@ -24,3 +24,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Worst parity margin of each group of checks (printed on success too)."""
+    try:
+        import _parity
+    except Exception:  # pragma: no cover
+        return
+    lines = _parity.summary_lines()
+    if lines:
+        terminalreporter.section("parity margins (error / bound; 1.00 = at the bound)")
+        for ln in lines:
+            terminalreporter.write_line(ln)

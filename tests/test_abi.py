@@ -103,3 +103,8 @@ def test_binding_fails_loudly_without_library(tmp_path):
     from speculative_decoding_draft_eagle_gb300 import _lib
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_debug_inject_rejects_unknown_bits(L):
+    assert L.stt_debug_inject(0x80) == -1
+    assert L.stt_debug_inject(0) == 0

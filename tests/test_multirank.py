@@ -33,8 +33,8 @@ def _worker(rank, world, port, out):
     import bench
     t = 10.0 + rank          # per-rank elapsed time
     work = 100.0 * (rank + 1)  # per-rank units
-    mx = bench.allreduce_max(t, world, "cpu")
-    sm = bench.allreduce_sum(work, world, "cpu")
+    mx = bench.allreduce(t, world, "cpu", "max")
+    sm = bench.allreduce(work, world, "cpu", "sum")
     bench.barrier(world)
     out[rank] = (mx, sm)
     dist.destroy_process_group()
@@ -61,3 +61,12 @@ def test_reference_arm_runs_on_rank0_only():
                        timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_gpus_flag_must_match_the_launch():
+    """--gpus N without N ranks is refused instead of silently running one."""
+    env = dict(os.environ)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--steps", "1"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "WORLD_SIZE" in (r.stderr + r.stdout)

@@ -54,6 +54,7 @@ def _same(a, b):
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
+    from oracle import soft_ce as osc
     from speculative_decoding_draft_eagle_gb300 import _lib, build, workloads as wl
     build.build()
     L = _lib.lib()
@@ -67,6 +68,12 @@ def test_noalloc_matches_workspace_entry_point_twice():
         _same(z2, z1)
         _same(r2, r1)
         assert abs(l2.item() - l1.item()) <= 1e-5 * abs(l1.item())
+        # and against the fp64 oracle directly, so that a fault shared by both
+        # entry points would not pass unseen
+        Lr, rlr, gr = osc.soft_ce(z.cpu().numpy(), p.cpu().numpy(), g.cpu().numpy())
+        _same(z2, torch.from_numpy(gr))
+        _same(r2, torch.from_numpy(rlr))
+        assert abs(l2.item() - Lr) <= 1e-5 * abs(Lr)
 
 
 def test_noalloc_rejects_too_many_rows():
