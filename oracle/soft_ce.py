@@ -13,8 +13,10 @@ gradient g [N]:
 
 and the scalar returned is L = sum_r g_r * l_r, whose derivative with respect to
 z is exactly ``grad`` (when sum(p) = 1 this is g*(pi - p), §四).  g is read as
-one value per row (the loss mask divided by N in the workloads); the formula
-also admits one value per element, which is not built.
+one value per row (the loss mask divided by N in the workloads).  The formula
+s = sum(p * g) also admits one value per element, G [N, V]; that reading is
+``soft_ce_elementwise``: the loss is L = -sum_rv G_rv p_rv log pi_rv, whose
+z-gradient is again -(p*G - pi*s) with s_r = sum_v p_rv G_rv.
 
 The per-row loss reported for a row with g_r = 0 is 0: that row is masked out
 of the loss, and its gradient is exactly 0 (convention; parity unpinned).
@@ -69,3 +71,34 @@ def soft_ce_row(z_row, p_row, g_r):
         s += float(p_row[v]) * float(g_r)
     grad = [-(float(p_row[v]) * float(g_r) - np.exp(float(z_row[v]) - lse) * s) for v in range(V)]
     return (ell if g_r != 0.0 else 0.0), np.array(grad)
+
+
+def soft_ce_elementwise(z, p, G):
+    """Per-element upstream gradient G [N, V] (SpecForge review, §三 "内存高效梯度计算":
+    s = sum(p * g) with g of the logits' shape).  Return (L, row_loss [N], grad [N,V]):
+
+        pi = softmax(z_r),  lse_r = log sum_v exp(z_rv)
+        row_loss_r = -sum_v G_rv p_rv log pi_rv = sum_v G_rv p_rv (lse_r - z_rv)
+        s_r = sum_v p_rv G_rv,  grad_rv = -(p_rv G_rv - pi_rv s_r)
+        L = sum_r row_loss_r
+
+    With G_rv = g_r for every v this is ``soft_ce`` (row_loss then carries the
+    weight g_r).  Float64, rows in chunks."""
+    z = np.asarray(z, dtype=np.float64)
+    p = np.asarray(p, dtype=np.float64)
+    G = np.asarray(G, dtype=np.float64)
+    N, V = z.shape
+    grad = np.empty((N, V))
+    row_loss = np.zeros(N)
+    for r0 in range(0, N, _CHUNK_ROWS):
+        r1 = min(N, r0 + _CHUNK_ROWS)
+        zc, pc, Gc = z[r0:r1], p[r0:r1], G[r0:r1]
+        m = zc.max(axis=1)
+        lse = m + np.log(np.exp(zc - m[:, None]).sum(axis=1))
+        log_pi = zc - lse[:, None]
+        pi = np.exp(log_pi)
+        pg = pc * Gc
+        row_loss[r0:r1] = -(pg * log_pi).sum(axis=1)
+        s = pg.sum(axis=1)
+        grad[r0:r1] = -(pg - pi * s[:, None])
+    return float(row_loss.sum()), row_loss, grad

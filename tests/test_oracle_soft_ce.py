@@ -135,3 +135,67 @@ def test_planted_sign_slip_is_caught(monkeypatch):
     pi /= pi.sum(1, keepdims=True)
     np.testing.assert_allclose(good, g[:, None] * (pi - p), atol=1e-15)
     assert not np.allclose(-good, g[:, None] * (pi - p), atol=1e-6)
+
+
+# ------------------------------------------------ per-element g (variant) --
+
+def test_elementwise_golden_hand_rows():
+    rows, L = [], None
+    for line in open(os.path.join(GOLDEN, "soft_ce_elementwise_hand.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        vals = [float(x) for x in line.split()]
+        if len(vals) == 1:
+            L = vals[0]
+        else:
+            rows.append(vals)
+    a = np.array(rows)
+    Lo, rl, grad = osc.soft_ce_elementwise(a[:, 0:2], a[:, 2:4], a[:, 4:6])
+    np.testing.assert_allclose(rl, a[:, 6], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(grad, a[:, 7:9], rtol=0, atol=1e-14)
+    assert abs(Lo - L) < 1e-14
+
+
+def test_elementwise_with_row_constant_g_is_the_per_row_form():
+    z, p, g = _rand(17, 45, 8, sum_p_one=False)
+    L1, rl1, gr1 = osc.soft_ce(z, p, g)
+    L2, rl2, gr2 = osc.soft_ce_elementwise(z, p, np.repeat(g[:, None], 45, axis=1))
+    assert abs(L1 - L2) <= 1e-13 * abs(L1)
+    np.testing.assert_allclose(rl2, g * rl1, rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(gr2, gr1, rtol=0, atol=1e-15)
+
+
+def test_elementwise_finite_differences():
+    r = np.random.default_rng(9)
+    z, p, _ = _rand(3, 7, 10, sum_p_one=False)
+    G = r.uniform(0.0, 2.0, size=z.shape)
+    _, _, grad = osc.soft_ce_elementwise(z, p, G)
+    h = 1e-6
+    num = np.zeros_like(z)
+    for i in range(z.shape[0]):
+        for j in range(z.shape[1]):
+            zp, zm = z.copy(), z.copy()
+            zp[i, j] += h
+            zm[i, j] -= h
+            num[i, j] = (osc.soft_ce_elementwise(zp, p, G)[0] - osc.soft_ce_elementwise(zm, p, G)[0]) / (2 * h)
+    np.testing.assert_allclose(grad, num, rtol=1e-7, atol=1e-9)
+    np.testing.assert_allclose(grad.sum(1), 0.0, atol=1e-14)
+
+
+def test_elementwise_one_hot_is_cross_entropy_weighted_at_the_target():
+    r = np.random.default_rng(11)
+    N, V = 12, 30
+    z = 2.0 * r.standard_normal((N, V))
+    t = r.integers(0, V, size=N)
+    p = np.zeros((N, V))
+    p[np.arange(N), t] = 1.0
+    G = r.uniform(0.0, 1.0, size=(N, V))
+    L, rl, grad = osc.soft_ce_elementwise(z, p, G)
+    zt = torch.tensor(z, requires_grad=True)
+    ce = F.cross_entropy(zt, torch.tensor(t), reduction="none")
+    w = torch.tensor(G[np.arange(N), t])
+    (ce * w).sum().backward()
+    np.testing.assert_allclose(rl, (ce * w).detach().numpy(), rtol=1e-12)
+    assert abs(L - float((ce * w).sum())) <= 1e-12 * abs(L)
+    np.testing.assert_allclose(grad, zt.grad.numpy(), rtol=0, atol=1e-14)
