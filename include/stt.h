@@ -153,13 +153,50 @@ STT_API size_t stt_attn_bwd_workspace_size(int B, int H, int H_kv, int D, int Q_
  *           group; zero for rows no query sees).
  *  dv_blocks same for dL/dV_j.
  *  workspace device scratch of at least stt_attn_bwd_workspace_size() bytes,
- *           16-byte aligned; contents on entry are ignored.
+ *           256-byte aligned; contents on entry are ignored.
  * ------------------------------------------------------------------------ */
 STT_API int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
                  const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
                  float scale, const void* out, const void* dout, const float* lse, float* dq,
                  float* const* dk_blocks, float* const* dv_blocks, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * Sparse-tree attention, backward with options.  Same operation and
+ * arguments as stt_attn_bwd, plus `flags`:
+ *
+ *  STT_BWD_ACCUMULATE_KV  dL/dK_j and dL/dV_j are ADDED to what dk_blocks[j]
+ *           and dv_blocks[j] hold instead of overwriting them (dq is still
+ *           overwritten).  This is the training use of the TTT step loop
+ *           (SpecForge review, §三 "稀疏树注意力", TTT length 7, and §六
+ *           "训练时测试（TTT）长度的影响"): block j is read by every step k >= j,
+ *           so its gradient is the sum over those steps; each step's call adds
+ *           its part in place, with no separate pass over the block gradients.
+ *           Rows that no query of the step sees are left unchanged.
+ *  STT_BWD_BF16_GRADS  dq, dk_blocks[j] and dv_blocks[j] are bf16 (round to
+ *           nearest even) instead of fp32.  Sums across key tiles and heads
+ *           are taken in fp32 in the workspace and rounded once at the end;
+ *           with STT_BWD_ACCUMULATE_KV the existing bf16 value is added in fp32
+ *           and the sum rounded once per call.
+ *
+ *  dq, dk_blocks, dv_blocks  device pointers of the element type the flags
+ *           select, layouts as in stt_attn_bwd.
+ *  workspace at least stt_attn_bwd_ex_workspace_size(..., flags) bytes,
+ *           256-byte aligned (STT_ERR_MISALIGNED otherwise); contents on entry
+ *           are ignored.
+ * Unknown flag bits return STT_ERR_INVALID_ARG.  stt_attn_bwd is this call
+ * with flags = 0.
+ * ------------------------------------------------------------------------ */
+#define STT_BWD_ACCUMULATE_KV 0x1u
+#define STT_BWD_BF16_GRADS 0x2u
+STT_API size_t stt_attn_bwd_ex_workspace_size(int B, int H, int H_kv, int D, int Q_LEN, int k,
+                                              uint32_t flags);
+STT_API int stt_attn_bwd_ex(const void* q, const void* const* k_blocks,
+                            const void* const* v_blocks, const int32_t* T_host, int B, int H,
+                            int H_kv, int D, int Q_LEN, int k, float scale, const void* out,
+                            const void* dout, const float* lse, void* dq, void* const* dk_blocks,
+                            void* const* dv_blocks, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace soft_ce_fwd_bwd_inplace needs (>= 16). */
 STT_API size_t soft_ce_workspace_size(int64_t N, int64_t V);
@@ -183,6 +220,33 @@ STT_API size_t soft_ce_workspace_size(int64_t N, int64_t V);
 STT_API int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, int64_t N, int64_t V,
                             float* row_loss, float* loss, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * Soft-CE variants the formula admits (SpecForge review, §三 "内存高效梯度计算":
+ * s = sum(p * g), z <- -(p * g - pi * s)).  `flags`:
+ *
+ *  STT_CE_BF16           z and p are bf16 [N, V]; every sum is taken in fp32
+ *                        and the gradient is written over z rounded to bf16
+ *                        (nearest even).
+ *  STT_CE_G_PER_ELEMENT  g is fp32 [N, V], one upstream gradient per logit:
+ *                            s_r = sum_v p_rv g_rv,  z_rv <- pi_rv s_r - p_rv g_rv,
+ *                            row_loss_r = -sum_v g_rv p_rv log pi_rv,
+ *                            L = sum_r row_loss_r
+ *                        (row_loss is then already weighted, and every row is
+ *                        read).
+ * flags = 0 is soft_ce_fwd_bwd_inplace (fp32 z and p, per-row g).  Other
+ * arguments, the workspace and the status codes as there; V may be at most
+ * 16 slices of the shared memory a CTA can hold (above ~270000 for fp32 with
+ * a per-element g) and STT_ERR_UNSUPPORTED is returned beyond that.  Unknown
+ * flag bits return STT_ERR_INVALID_ARG.  Rows whose addresses are 16-byte
+ * aligned with V % 8 == 0 take bulk copies; others an element-wise path with
+ * identical results.
+ * ------------------------------------------------------------------------ */
+#define STT_CE_BF16 0x1u
+#define STT_CE_G_PER_ELEMENT 0x2u
+STT_API int soft_ce_fwd_bwd_inplace_ex(void* z, const void* p, const float* g, int64_t N,
+                                       int64_t V, uint32_t flags, float* row_loss, float* loss,
+                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
  * Allocation-free soft-CE (the paper has no counterpart; this is a library
@@ -237,6 +301,8 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_KERNEL_ATTN_FWD 3
 #define STT_KERNEL_ATTN_BWD_PREP 4
 #define STT_KERNEL_ATTN_BWD_CAUSAL 5
+#define STT_KERNEL_ATTN_BWD_CAST 6
+#define STT_KERNEL_SOFT_CE_VARIANT 7
 
 /* Device error-word bits: sites of bounded waits that gave up, and blocks
  * whose dynamic shared memory did not have the 1024-byte alignment the

@@ -33,8 +33,11 @@ EXPORTS = (
     "stt_attn_fwd",
     "stt_attn_bwd_workspace_size",
     "stt_attn_bwd",
+    "stt_attn_bwd_ex_workspace_size",
+    "stt_attn_bwd_ex",
     "soft_ce_workspace_size",
     "soft_ce_fwd_bwd_inplace",
+    "soft_ce_fwd_bwd_inplace_ex",
     "soft_ce_fwd_bwd_inplace_noalloc",
     "stt_profile_start",
     "stt_profile_stop",
@@ -73,10 +76,18 @@ def _declare(L):
                                i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp,
                                c.POINTER(vp), c.POINTER(vp), vp, sz, vp]
     L.stt_attn_bwd.restype = i32
+    L.stt_attn_bwd_ex_workspace_size.argtypes = [i32] * 6 + [c.c_uint32]
+    L.stt_attn_bwd_ex_workspace_size.restype = sz
+    L.stt_attn_bwd_ex.argtypes = [vp, c.POINTER(vp), c.POINTER(vp), c.POINTER(c.c_int32),
+                                  i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp,
+                                  c.POINTER(vp), c.POINTER(vp), c.c_uint32, vp, sz, vp]
+    L.stt_attn_bwd_ex.restype = i32
     L.soft_ce_workspace_size.argtypes = [i64, i64]
     L.soft_ce_workspace_size.restype = sz
     L.soft_ce_fwd_bwd_inplace.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
     L.soft_ce_fwd_bwd_inplace.restype = i32
+    L.soft_ce_fwd_bwd_inplace_ex.argtypes = [vp, vp, vp, i64, i64, c.c_uint32, vp, vp, vp, sz, vp]
+    L.soft_ce_fwd_bwd_inplace_ex.restype = i32
     L.soft_ce_fwd_bwd_inplace_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]
     L.soft_ce_fwd_bwd_inplace_noalloc.restype = i32
     L.stt_profile_start.argtypes = [i32]

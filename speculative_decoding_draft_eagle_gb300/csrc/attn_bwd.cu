@@ -49,14 +49,38 @@ struct BwdParams {
   const __nv_bfloat16* out;
   const __nv_bfloat16* dout;
   const float* lse;
-  float* dq;
-  float* dkb[kMaxBlocks];
-  float* dvb[kMaxBlocks];
+  float* dq;                // fp32 dq accumulator (the caller's dq, or workspace)
+  void* dkb[kMaxBlocks];    // the caller's dK_j / dV_j (fp32, or bf16 with kBwdBf16)
+  void* dvb[kMaxBlocks];
+  float* dk0;               // fp32 accumulators of dK_0 / dV_0 (the caller's, or workspace)
+  float* dv0;
   float* delta;
   int B, H, H_kv, Q_LEN, k, n_t, G;
+  int accumulate;           // add into dK_j / dV_j, j >= 1 (read-modify-write)
+  int zero_acc0;            // the prep kernel zeroes dk0 / dv0 first
   float scale, scale_log2;
   int T[kMaxBatch];
 };
+
+// Byte offsets of the workspace parts, each 256-byte aligned.
+struct WorkspaceLayout {
+  size_t delta, dq, dk0, dv0, total;
+};
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+inline WorkspaceLayout workspace_layout(int B, int H, int H_kv, int D, int Q_LEN, uint32_t flags) {
+  WorkspaceLayout W{};
+  W.delta = 0;
+  W.total = align256((size_t)B * H * Q_LEN * sizeof(float));
+  if (flags & kBwdBf16) {
+    W.dq = W.total;
+    W.total += align256((size_t)B * H * Q_LEN * D * sizeof(float));
+    W.dk0 = W.total;
+    W.total += align256((size_t)B * H_kv * Q_LEN * D * sizeof(float));
+    W.dv0 = W.total;
+    W.total += align256((size_t)B * H_kv * Q_LEN * D * sizeof(float));
+  }
+  return W;
+}
 
 // Sum over the L lanes of an aligned lane group (L a power of two <= 32).
 template <int L>
@@ -129,6 +153,51 @@ __device__ __forceinline__ void store_vec(float* p, const float (&v)[E], bool st
   }
 }
 
+// E fp32 values of a gradient row into fp32 (OUT = float) or bf16 (OUT =
+// __nv_bfloat16, rounded to nearest even) memory at `p`; with `acc` the values
+// are added to what is there (in fp32, then rounded once).
+template <typename OUT, int E>
+__device__ __forceinline__ void put_grad(void* base, size_t off, const float (&v)[E], bool acc) {
+  if constexpr (sizeof(OUT) == 4) {
+    float* p = static_cast<float*>(base) + off;
+    if (!acc) {
+      store_vec<E>(p, v, true);
+      return;
+    }
+    float4* p4 = reinterpret_cast<float4*>(p);
+#pragma unroll
+    for (int i = 0; i < E / 4; ++i) {
+      float4 x = p4[i];
+      x.x += v[4 * i];
+      x.y += v[4 * i + 1];
+      x.z += v[4 * i + 2];
+      x.w += v[4 * i + 3];
+      p4[i] = x;
+    }
+  } else {
+    static_assert(E == 8, "bf16 gradient rows are written 16 bytes at a time");
+    uint4* p4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
+    float w[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) w[e] = v[e];
+    if (acc) {
+      const uint4 x = *p4;
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[2 * i] += bf16lo(xs[i]);
+        w[2 * i + 1] += bf16hi(xs[i]);
+      }
+    }
+    const uint4 y = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]),
+                               pack_bf16(w[6], w[7]));
+    if (acc)
+      *p4 = y;
+    else
+      __stcs(p4, y);
+  }
+}
+
 // Row r, 16-byte chunk w of a swizzled [128 rows x 128 bytes] staging block.
 __device__ __forceinline__ uint32_t swz128(int r, int w) {
   return (uint32_t)(r * 128 + ((w ^ (r & 7)) << 4));
@@ -155,7 +224,7 @@ struct PrepShape {
   static constexpr int kMinBlocks = GH <= 2 ? 2 : 3;
 };
 
-template <int D, int GM>
+template <int D, int GM, typename OUT>
 __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBlocks)
     attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
   constexpr int E = PrepShape<GM>::E;
@@ -248,6 +317,9 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
             dv[e] = fmaf(p, vec_at<E>(dov[i], e), dv[e]);
           }
         }
+        // Rows without suffix keys add nothing: written as zeros when the
+        // gradients are overwritten, left alone when they are accumulated.
+        const bool put = live && (valid || !P.accumulate);
         if constexpr (SH == 2) {
           // The other half-warp holds the group's other heads: sum, then
           // half-warp 0 stores dK_j and half-warp 1 dV_j.
@@ -259,10 +331,10 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
           float out[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) out[e] = hh == 0 ? dk[e] : dv[e];
-          if (live) store_vec<E>((hh == 0 ? P.dkb[j] : P.dvb[j]) + kvoff, out, true);
-        } else if (live) {
-          store_vec<E>(P.dkb[j] + kvoff, dk, true);
-          store_vec<E>(P.dvb[j] + kvoff, dv, true);
+          if (put) put_grad<OUT, E>(hh == 0 ? P.dkb[j] : P.dvb[j], kvoff, out, P.accumulate != 0);
+        } else if (put) {
+          put_grad<OUT, E>(P.dkb[j], kvoff, dk, P.accumulate != 0);
+          put_grad<OUT, E>(P.dvb[j], kvoff, dv, P.accumulate != 0);
         }
       }
     }
@@ -272,11 +344,13 @@ __global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBl
         if (hh * GH + i < G)
           store_vec<E>(P.dq + ((size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q) * D + li * E,
                        dq[i], false);
-      float z[E];
+      if (P.zero_acc0) {
+        float z[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) z[e] = 0.f;
-      if (SH == 1 || hh == 0) store_vec<E>(P.dkb[0] + kvoff, z, false);
-      if (SH == 1 || hh == 1) store_vec<E>(P.dvb[0] + kvoff, z, false);
+        for (int e = 0; e < E; ++e) z[e] = 0.f;
+        if (SH == 1 || hh == 0) store_vec<E>(P.dk0 + kvoff, z, false);
+        if (SH == 1 || hh == 1) store_vec<E>(P.dv0 + kvoff, z, false);
+      }
     }
   }
 }
@@ -807,19 +881,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ cast --
+// bf16 gradients: dq, dK_0 and dV_0 were accumulated in fp32 in the workspace;
+// round them to the caller's bf16 buffers (dK_0 / dV_0 added to the values
+// already there when accumulating).  n4 groups of four elements per tensor.
+struct CastParams {
+  const float* src[3];
+  __nv_bfloat16* dst[3];
+  long long n4[3];
+  int accumulate_kv;  // tensors 1 and 2 (dK_0, dV_0) add to dst
+};
+
+__global__ void __launch_bounds__(256) attn_bwd_cast_kernel(const __grid_constant__ CastParams C) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+#pragma unroll 1
+  for (int t = 0; t < 3; ++t) {
+    const float4* src = reinterpret_cast<const float4*>(C.src[t]);
+    uint2* dst = reinterpret_cast<uint2*>(C.dst[t]);
+    const bool acc = t > 0 && C.accumulate_kv;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < C.n4[t]; i += stride) {
+      float4 v = __ldcs(src + i);
+      if (acc) {
+        const uint2 o = dst[i];
+        v.x += bf16lo(o.x);
+        v.y += bf16hi(o.x);
+        v.z += bf16lo(o.y);
+        v.w += bf16hi(o.y);
+      }
+      const uint2 y = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+      __stcs(dst + i, y);
+    }
+  }
+}
+
 template <int D, int GM>
-void launch_prep(const BwdParams& P, cudaStream_t s) {
+void launch_prep(const BwdParams& P, bool bf16, cudaStream_t s) {
   const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
   using S = PrepShape<GM>;
   const long long per_block = (S::kThreads / 32) * (32 / S::SH / (D / S::E));
   long long blocks = (rows + per_block - 1) / per_block;
   if (blocks > 152 * 64) blocks = 152 * 64;  // grid-stride beyond that
-  attn_bwd_prep_kernel<D, GM><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
+  if (bf16)
+    attn_bwd_prep_kernel<D, GM, __nv_bfloat16><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
+  else
+    attn_bwd_prep_kernel<D, GM, float><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
 }
 
 template <int D>
 cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   static thread_local BwdParams P;
+  const bool bf16 = (g.flags & kBwdBf16) != 0;
+  const bool acc = (g.flags & kBwdAccumulate) != 0;
+  const WorkspaceLayout W = workspace_layout(a.B, a.H, a.H_kv, D, a.Q_LEN, g.flags);
+  unsigned char* ws = static_cast<unsigned char*>(g.workspace);
   P.q = static_cast<const __nv_bfloat16*>(a.q);
   for (int j = 0; j < kMaxBlocks; ++j) {
     P.kb[j] = static_cast<const __nv_bfloat16*>(a.k_blocks[j]);
@@ -830,8 +944,20 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   P.out = static_cast<const __nv_bfloat16*>(g.out);
   P.dout = static_cast<const __nv_bfloat16*>(g.dout);
   P.lse = g.lse;
-  P.dq = g.dq;
-  P.delta = g.delta;
+  P.delta = reinterpret_cast<float*>(ws + W.delta);
+  if (bf16) {
+    P.dq = reinterpret_cast<float*>(ws + W.dq);
+    P.dk0 = reinterpret_cast<float*>(ws + W.dk0);
+    P.dv0 = reinterpret_cast<float*>(ws + W.dv0);
+  } else {
+    P.dq = static_cast<float*>(g.dq);
+    P.dk0 = static_cast<float*>(g.dk_blocks[0]);
+    P.dv0 = static_cast<float*>(g.dv_blocks[0]);
+  }
+  P.accumulate = acc ? 1 : 0;
+  // fp32 accumulation adds straight into the caller's dK_0 / dV_0; otherwise
+  // the accumulators start at zero.
+  P.zero_acc0 = (acc && !bf16) ? 0 : 1;
   P.B = a.B;
   P.H = a.H;
   P.H_kv = a.H_kv;
@@ -852,21 +978,19 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   if ((e = encode_tile_map(&tmV, a.v_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
     return e;
   CUtensorMap tmDQ, tmDK, tmDV;
-  if ((e = encode_f32_map(&tmDQ, g.dq, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
-  if ((e = encode_f32_map(&tmDK, g.dk_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
-    return e;
-  if ((e = encode_f32_map(&tmDV, g.dv_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)
-    return e;
+  if ((e = encode_f32_map(&tmDQ, P.dq, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
+  if ((e = encode_f32_map(&tmDK, P.dk0, D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess) return e;
+  if ((e = encode_f32_map(&tmDV, P.dv0, D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess) return e;
 
   prof_before(s, STT_KERNEL_ATTN_BWD_PREP);
   if (P.G == 1)
-    launch_prep<D, 1>(P, s);
+    launch_prep<D, 1>(P, bf16, s);
   else if (P.G == 2)
-    launch_prep<D, 2>(P, s);
+    launch_prep<D, 2>(P, bf16, s);
   else if (P.G <= 4)
-    launch_prep<D, 4>(P, s);
+    launch_prep<D, 4>(P, bf16, s);
   else
-    launch_prep<D, 8>(P, s);
+    launch_prep<D, 8>(P, bf16, s);
   prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -878,13 +1002,31 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   attn_bwd_causal_kernel<D><<<grid, kThreads, CausalSmem<D>::alloc, s>>>(P, tmQ, tmDO, tmK, tmV,
                                                                         tmDQ, tmDK, tmDV);
   prof_after(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!bf16) return cudaSuccess;
+
+  CastParams C;
+  C.src[0] = P.dq;
+  C.src[1] = P.dk0;
+  C.src[2] = P.dv0;
+  C.dst[0] = static_cast<__nv_bfloat16*>(g.dq);
+  C.dst[1] = static_cast<__nv_bfloat16*>(g.dk_blocks[0]);
+  C.dst[2] = static_cast<__nv_bfloat16*>(g.dv_blocks[0]);
+  C.n4[0] = (long long)a.B * a.H * a.Q_LEN * D / 4;
+  C.n4[1] = C.n4[2] = (long long)a.B * a.H_kv * a.Q_LEN * D / 4;
+  C.accumulate_kv = acc ? 1 : 0;
+  long long blocks = (C.n4[0] + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  prof_before(s, STT_KERNEL_ATTN_BWD_CAST);
+  attn_bwd_cast_kernel<<<(unsigned)blocks, 256, 0, s>>>(C);
+  prof_after(s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t attn_bwd_workspace(int B, int H, int Q_LEN) {
-  return ((size_t)B * H * Q_LEN * sizeof(float) + 15) / 16 * 16;
+size_t attn_bwd_workspace(int B, int H, int H_kv, int D, int Q_LEN, uint32_t flags) {
+  return workspace_layout(B, H, H_kv, D, Q_LEN, flags).total;
 }
 
 cudaError_t attn_bwd_launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {

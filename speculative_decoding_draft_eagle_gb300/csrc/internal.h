@@ -23,6 +23,27 @@ constexpr int64_t kCeMaxV = 409600;  // 16 CTAs x 25600 elements
 cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const float* g, int64_t N,
                            int64_t V, float* row_loss, float* loss, float* wl, cudaStream_t s);
 
+// Fixed-order sum of the per-row weighted losses wl[0..N) into *loss, launched
+// as a programmatic dependent of the kernel before it on the stream.
+cudaError_t soft_ce_loss_sum_launch(const float* wl, int64_t N, float* loss, cudaStream_t s);
+
+// Variants (the STT_CE_* bits of the public header).
+constexpr uint32_t kCeBf16 = 0x1u;         // z and p are bf16
+constexpr uint32_t kCeGPerElement = 0x2u;  // g is fp32 [N, V]
+struct CeVariantPlan {
+  bool ok;     // the slice fits in shared memory
+  bool bulk;   // 16-byte aligned rows (bulk copies)
+  int C;       // CTAs per row (cluster size)
+  int slice;   // elements per CTA
+  int chunk;   // elements per bulk-copy chunk
+  int smem;    // dynamic shared bytes per CTA
+};
+CeVariantPlan soft_ce_variant_plan(const void* z, const void* p, const float* g, int64_t V,
+                                   uint32_t flags);
+cudaError_t soft_ce_variant_launch(const CeVariantPlan& plan, uint32_t flags, void* z,
+                                   const void* p, const float* g, int64_t N, int64_t V,
+                                   float* row_loss, float* loss, float* wl, cudaStream_t s);
+
 // ----------------------------------------------------------- attention ----
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxBlocks = 32;
@@ -38,16 +59,23 @@ struct AttnArgs {
 
 cudaError_t attn_fwd_launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s);
 
+// Flags of the backward (the STT_BWD_* bits of the public header).
+constexpr uint32_t kBwdAccumulate = 0x1u;  // add into dK_j / dV_j instead of overwriting
+constexpr uint32_t kBwdBf16 = 0x2u;        // dq, dK_j, dV_j are bf16
+
 struct AttnBwdArgs {
   const void* out;
   const void* dout;
   const float* lse;
-  float* dq;
-  float* dk_blocks[kMaxBlocks];
-  float* dv_blocks[kMaxBlocks];
-  float* delta;  // workspace: [B, H, Q_LEN] fp32
+  void* dq;                     // fp32, or bf16 with kBwdBf16
+  void* dk_blocks[kMaxBlocks];  // same element type as dq
+  void* dv_blocks[kMaxBlocks];
+  uint32_t flags;
+  void* workspace;  // attn_bwd_workspace(...) bytes, 256-byte aligned
 };
-size_t attn_bwd_workspace(int B, int H, int Q_LEN);
+// Workspace: Delta [B, H, Q_LEN] fp32; with kBwdBf16 also fp32 accumulators
+// for dq [B, H, Q_LEN, D] and dK_0, dV_0 [B, H_kv, Q_LEN, D].
+size_t attn_bwd_workspace(int B, int H, int H_kv, int D, int Q_LEN, uint32_t flags);
 cudaError_t attn_bwd_launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s);
 
 // Per-file device error words (read and cleared).

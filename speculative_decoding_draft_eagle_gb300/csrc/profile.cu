@@ -98,6 +98,8 @@ const char* stt_kernel_name(int kernel_id) {
     case STT_KERNEL_ATTN_FWD: return "attn_fwd";
     case STT_KERNEL_ATTN_BWD_PREP: return "attn_bwd_prep";
     case STT_KERNEL_ATTN_BWD_CAUSAL: return "attn_bwd_causal";
+    case STT_KERNEL_ATTN_BWD_CAST: return "attn_bwd_cast";
+    case STT_KERNEL_SOFT_CE_VARIANT: return "soft_ce_variant";
     default: return "unknown";
   }
 }

@@ -798,6 +798,13 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
   // The loss sum follows the row kernel directly (no profiling event between
   // them, which would serialise the pair), as a programmatic dependent launch;
   // the profiled unit STT_KERNEL_SOFT_CE covers both kernels.
+  const cudaError_t e2 = soft_ce_loss_sum_launch(wl, N, loss, s);
+  prof_after(s);
+  if (e2 != cudaSuccess) return e2;
+  return cudaGetLastError();
+}
+
+cudaError_t soft_ce_loss_sum_launch(const float* wl, int64_t N, float* loss, cudaStream_t s) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(1, 1, 1);
   lc.blockDim = dim3(1024, 1, 1);
@@ -808,10 +815,7 @@ cudaError_t soft_ce_launch(const CePlan& plan, float* z, const float* p, const f
   la[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = la;
   lc.numAttrs = 1;
-  const cudaError_t e2 = cudaLaunchKernelEx(&lc, soft_ce_loss_sum, wl, (long long)N, loss);
-  prof_after(s);
-  if (e2 != cudaSuccess) return e2;
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&lc, soft_ce_loss_sum, wl, (long long)N, loss);
 }
 
 STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)

@@ -41,6 +41,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int from_cuda(cudaError_t e) { return stt::status_from_cuda(e); }
 
 static_assert(STT_ERR_UNSUPPORTED == -2 && STT_ERR_CUDA == -4, "status_from_cuda codes");
+static_assert(STT_CE_BF16 == stt::kCeBf16 && STT_CE_G_PER_ELEMENT == stt::kCeGPerElement,
+              "soft-CE flags");
+static_assert(STT_BWD_ACCUMULATE_KV == stt::kBwdAccumulate && STT_BWD_BF16_GRADS == stt::kBwdBf16,
+              "backward flags");
 
 // Shared validation of the attention arguments; fills `a` on success.
 int check_attn(const void* q, const void* const* k_blocks, const void* const* v_blocks,
@@ -141,22 +145,26 @@ int stt_attn_fwd(const void* q, const void* const* k_blocks, const void* const* 
 }
 
 size_t stt_attn_bwd_workspace_size(int B, int H, int H_kv, int D, int Q_LEN, int k) {
-  (void)H_kv;
-  (void)D;
-  (void)k;
-  if (B < 1 || H < 1 || Q_LEN < 1) return 16;
-  return stt::attn_bwd_workspace(B, H, Q_LEN);
+  return stt_attn_bwd_ex_workspace_size(B, H, H_kv, D, Q_LEN, k, 0u);
 }
 
-int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
-                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
-                 float scale, const void* out, const void* dout, const float* lse, float* dq,
-                 float* const* dk_blocks, float* const* dv_blocks, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+size_t stt_attn_bwd_ex_workspace_size(int B, int H, int H_kv, int D, int Q_LEN, int k,
+                                      uint32_t flags) {
+  (void)k;
+  if (B < 1 || H < 1 || H_kv < 1 || Q_LEN < 1 || D < 1) return 16;
+  return stt::attn_bwd_workspace(B, H, H_kv, D, Q_LEN, flags);
+}
+
+int stt_attn_bwd_ex(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                    const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                    float scale, const void* out, const void* dout, const float* lse, void* dq,
+                    void* const* dk_blocks, void* const* dv_blocks, uint32_t flags,
+                    void* workspace, size_t workspace_bytes, void* stream) {
   try {
     static thread_local stt::AttnArgs a;
     int st = check_attn(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, &a);
     if (st != STT_OK) return st;
+    if (flags & ~(uint32_t)(STT_BWD_ACCUMULATE_KV | STT_BWD_BF16_GRADS)) return STT_ERR_INVALID_ARG;
     if (!out || !dout || !lse || !dq || !dk_blocks || !dv_blocks) return STT_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq))
       return STT_ERR_MISALIGNED;
@@ -168,18 +176,30 @@ int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* 
       g.dk_blocks[j] = dk_blocks[j];
       g.dv_blocks[j] = dv_blocks[j];
     }
-    const size_t need = stt::attn_bwd_workspace(B, H, Q_LEN);
+    const size_t need = stt::attn_bwd_workspace(B, H, H_kv, D, Q_LEN, flags);
     if (!workspace || workspace_bytes < need) return STT_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return STT_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return STT_ERR_MISALIGNED;
     g.out = out;
     g.dout = dout;
     g.lse = lse;
     g.dq = dq;
-    g.delta = static_cast<float*>(workspace);
+    g.flags = flags;
+    g.workspace = workspace;
     return from_cuda(stt::attn_bwd_launch(a, g, static_cast<cudaStream_t>(stream)));
   } catch (...) {
     return STT_ERR_CUDA;
   }
+}
+
+int stt_attn_bwd(const void* q, const void* const* k_blocks, const void* const* v_blocks,
+                 const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
+                 float scale, const void* out, const void* dout, const float* lse, float* dq,
+                 float* const* dk_blocks, float* const* dv_blocks, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return stt_attn_bwd_ex(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, out, dout,
+                         lse, dq, reinterpret_cast<void* const*>(dk_blocks),
+                         reinterpret_cast<void* const*>(dv_blocks), 0u, workspace,
+                         workspace_bytes, stream);
 }
 
 size_t soft_ce_workspace_size(int64_t N, int64_t V) {
@@ -206,6 +226,30 @@ int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, int64_t N,
     return from_cuda(stt::soft_ce_launch(plan, z, p, g, N, V, row_loss, loss,
                                          static_cast<float*>(workspace),
                                          static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+int soft_ce_fwd_bwd_inplace_ex(void* z, const void* p, const float* g, int64_t N, int64_t V,
+                               uint32_t flags, float* row_loss, float* loss, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  try {
+    if (flags & ~(uint32_t)(STT_CE_BF16 | STT_CE_G_PER_ELEMENT)) return STT_ERR_INVALID_ARG;
+    if (flags == 0)
+      return soft_ce_fwd_bwd_inplace(static_cast<float*>(z), static_cast<const float*>(p), g, N,
+                                     V, row_loss, loss, workspace, workspace_bytes, stream);
+    if (N < 0 || V < 1 || !loss) return STT_ERR_INVALID_ARG;
+    if (N > 0 && (!z || !p || !g)) return STT_ERR_INVALID_ARG;
+    if (N > 0 && V > INT64_MAX / N) return STT_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < soft_ce_workspace_size(N, V)) return STT_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0) return STT_ERR_MISALIGNED;
+    const stt::CeVariantPlan plan = stt::soft_ce_variant_plan(z, p, g, V, flags);
+    if (!plan.ok) return STT_ERR_UNSUPPORTED;
+    if (N * (int64_t)plan.C > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    return from_cuda(stt::soft_ce_variant_launch(plan, flags, z, p, g, N, V, row_loss, loss,
+                                                 static_cast<float*>(workspace),
+                                                 static_cast<cudaStream_t>(stream)));
   } catch (...) {
     return STT_ERR_CUDA;
   }

@@ -19,7 +19,10 @@ __all__ = [
     "stt_attn_fwd",
     "stt_attn_bwd",
     "stt_attn_bwd_workspace_size",
+    "stt_attn_bwd_ex",
+    "stt_attn_bwd_ex_workspace_size",
     "soft_ce_fwd_bwd_inplace",
+    "soft_ce_fwd_bwd_inplace_ex",
     "soft_ce_fwd_bwd_inplace_noalloc",
     "soft_ce_workspace_size",
     "stt_device_error",
@@ -140,6 +143,53 @@ def stt_attn_bwd(q: torch.Tensor, k_blocks: Sequence[torch.Tensor],
     return dq, dk_blocks, dv_blocks
 
 
+STT_BWD_ACCUMULATE_KV = 0x1
+STT_BWD_BF16_GRADS = 0x2
+
+
+def stt_attn_bwd_ex_workspace_size(B, H, H_kv, D, Q_LEN, k, flags) -> int:
+    return int(lib().stt_attn_bwd_ex_workspace_size(B, H, H_kv, D, Q_LEN, k, flags))
+
+
+def stt_attn_bwd_ex(q: torch.Tensor, k_blocks: Sequence[torch.Tensor],
+                    v_blocks: Sequence[torch.Tensor], T, out: torch.Tensor, dout: torch.Tensor,
+                    lse: torch.Tensor, dq: torch.Tensor, dk_blocks: Sequence[torch.Tensor],
+                    dv_blocks: Sequence[torch.Tensor], scale: Optional[float] = None,
+                    accumulate: bool = False, workspace: Optional[torch.Tensor] = None,
+                    stream=None):
+    """Backward of stt_attn_fwd into caller-given gradient buffers, all fp32 or all
+    bf16 (the dtype of ``dq`` selects STT_BWD_BF16_GRADS).  With ``accumulate``
+    the block gradients are added to dk_blocks / dv_blocks (STT_BWD_ACCUMULATE_KV);
+    dq is always overwritten."""
+    B, H, H_kv, D, Q_LEN, k, T_arr = _attn_dims(q, k_blocks, v_blocks, T)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _need(out, "out", torch.bfloat16, q.shape)
+    _need(dout, "dout", torch.bfloat16, q.shape)
+    _need(lse, "lse", torch.float32, (B, H, Q_LEN))
+    gd = dq.dtype
+    if gd not in (torch.float32, torch.bfloat16):
+        raise ValueError("gradients must be float32 or bfloat16")
+    _need(dq, "dq", gd, q.shape)
+    if len(dk_blocks) != k + 1 or len(dv_blocks) != k + 1:
+        raise ValueError("dk_blocks and dv_blocks must hold k+1 tensors")
+    kv_shape = (B, H_kv, Q_LEN, D)
+    for j in range(k + 1):
+        _need(dk_blocks[j], f"dk_blocks[{j}]", gd, kv_shape)
+        _need(dv_blocks[j], f"dv_blocks[{j}]", gd, kv_shape)
+    flags = (STT_BWD_ACCUMULATE_KV if accumulate else 0) | (
+        STT_BWD_BF16_GRADS if gd == torch.bfloat16 else 0)
+    need = stt_attn_bwd_ex_workspace_size(B, H, H_kv, D, Q_LEN, k, flags)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    st = lib().stt_attn_bwd_ex(_ptr(q), _ptr_array(k_blocks), _ptr_array(v_blocks), T_arr, B, H,
+                               H_kv, D, Q_LEN, k, scale, _ptr(out), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr_array(dk_blocks), _ptr_array(dv_blocks), flags,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    check("stt_attn_bwd_ex", st)
+    return dq, dk_blocks, dv_blocks
+
+
 def soft_ce_workspace_size(N: int, V: int) -> int:
     return int(lib().soft_ce_workspace_size(N, V))
 
@@ -172,6 +222,49 @@ def soft_ce_fwd_bwd_inplace(z: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     check("soft_ce_fwd_bwd_inplace", st)
+    return loss, row_loss
+
+
+STT_CE_BF16 = 0x1
+STT_CE_G_PER_ELEMENT = 0x2
+
+
+def soft_ce_fwd_bwd_inplace_ex(z: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
+                               row_loss: Optional[torch.Tensor] = None,
+                               loss: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None):
+    """In-place soft-CE in any of the admitted forms: z and p both fp32 or both
+    bf16 (STT_CE_BF16), g fp32 of shape [N] (per row) or [N, V] (per element,
+    STT_CE_G_PER_ELEMENT).  z is overwritten with dL/dz in its own dtype.
+    Returns (loss [1], row_loss [N])."""
+    if z.dim() != 2:
+        raise ValueError("z must be [N, V]")
+    N, V = z.shape
+    if z.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("z must be float32 or bfloat16")
+    _need(z, "z", z.dtype)
+    _need(p, "p", z.dtype, (N, V))
+    if g.dim() == 2:
+        _need(g, "g", torch.float32, (N, V))
+    else:
+        _need(g, "g", torch.float32, (N,))
+    flags = (STT_CE_BF16 if z.dtype == torch.bfloat16 else 0) | (
+        STT_CE_G_PER_ELEMENT if g.dim() == 2 else 0)
+    dev = z.device
+    if loss is None:
+        loss = torch.empty(1, device=dev, dtype=torch.float32)
+    if row_loss is None:
+        row_loss = torch.empty(N, device=dev, dtype=torch.float32)
+    _need(loss, "loss", torch.float32)
+    _need(row_loss, "row_loss", torch.float32, (N,))
+    need = soft_ce_workspace_size(N, V)
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib().soft_ce_fwd_bwd_inplace_ex(_ptr(z), _ptr(p), _ptr(g), N, V, flags, _ptr(row_loss),
+                                          _ptr(loss), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    check("soft_ce_fwd_bwd_inplace_ex", st)
     return loss, row_loss
 
 

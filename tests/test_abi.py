@@ -108,3 +108,25 @@ def test_binding_fails_loudly_without_library(tmp_path):
 def test_debug_inject_rejects_unknown_bits(L):
     assert L.stt_debug_inject(0x80) == -1
     assert L.stt_debug_inject(0) == 0
+
+
+def test_attn_bwd_ex_rejects_bad_flags_and_workspace(L):
+    good = 0x1000
+    kb = _ptrs([good, good])
+    args = (good, kb, kb, _T([5]), 1, 4, 2, 128, 8, 1, 0.1, good, good, good, good, kb, kb)
+    assert L.stt_attn_bwd_ex(*args, 0x4, good, 1 << 20, None) == -1    # unknown flag
+    assert L.stt_attn_bwd_ex(*args, 0x2, good, 16, None) == -6         # bf16 needs a larger workspace
+    assert L.stt_attn_bwd_ex(*args, 0x1, good + 16, 1 << 20, None) == -3  # not 256-byte aligned
+    small = L.stt_attn_bwd_ex_workspace_size(1, 4, 2, 128, 8, 1, 0)
+    big = L.stt_attn_bwd_ex_workspace_size(1, 4, 2, 128, 8, 1, 2)
+    assert small == L.stt_attn_bwd_workspace_size(1, 4, 2, 128, 8, 1)
+    assert big >= small + (4 + 2 + 2) * 8 * 128 * 4
+
+
+def test_soft_ce_ex_rejects_bad_arguments(L):
+    good = 0x1000
+    f = L.soft_ce_fwd_bwd_inplace_ex
+    assert f(good, good, good, 4, 10, 0x8, None, good, good, 1 << 20, None) == -1   # unknown flag
+    assert f(good, good, good, -1, 10, 0x1, None, good, good, 1 << 20, None) == -1
+    assert f(good, good, good, 4, 10, 0x1, None, good, None, 0, None) == -6
+    assert f(good, good, good, 4, 10_000_000, 0x2, None, good, good, 1 << 20, None) == -2
