@@ -76,6 +76,17 @@ STT_API const char* stt_status_string(int status);
 STT_API int stt_version(void);
 
 /*
+ * The cudaError_t code of the last CUDA failure (a status of STT_ERR_CUDA or
+ * STT_ERR_UNSUPPORTED from a CUDA call) of a library call made by the calling
+ * thread, 0 if none since the last read; reading clears it.  If `name` is not
+ * NULL it receives the code's static name (cudaGetErrorName).  Every
+ * launching entry point first clears an error that an earlier runtime call of
+ * the same thread left pending, so a failure reported by the library is its
+ * own.
+ */
+STT_API int stt_last_cuda_error(const char** name);
+
+/*
  * Reads and clears the device-side error word (bitwise OR of the STT_DEVERR_*
  * sites whose bounded wait ran out since the last call).  Synchronises
  * `stream` first, then stores the word in *word and returns STT_ERR_TIMEOUT

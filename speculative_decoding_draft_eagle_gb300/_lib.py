@@ -27,6 +27,7 @@ STATUS = {
 EXPORTS = (
     "stt_status_string",
     "stt_version",
+    "stt_last_cuda_error",
     "stt_device_error",
     "stt_debug_set_wait_budget",
     "stt_debug_inject",
@@ -61,6 +62,8 @@ def _declare(L):
     L.stt_status_string.restype = c.c_char_p
     L.stt_version.argtypes = []
     L.stt_version.restype = i32
+    L.stt_last_cuda_error.argtypes = [c.POINTER(c.c_char_p)]
+    L.stt_last_cuda_error.restype = i32
     L.stt_device_error.argtypes = [vp, c.POINTER(c.c_uint32)]
     L.stt_device_error.restype = i32
     L.stt_debug_set_wait_budget.argtypes = [c.c_uint64]
@@ -121,4 +124,8 @@ def lib():
 def check(fn: str, status: int):
     if status != 0:
         msg = lib().stt_status_string(status).decode()
+        name = ctypes.c_char_p()
+        code = lib().stt_last_cuda_error(ctypes.byref(name))
+        if code:
+            msg += f"; CUDA error {code} {name.value.decode() if name.value else ''}"
         raise SttError(fn, status, msg)

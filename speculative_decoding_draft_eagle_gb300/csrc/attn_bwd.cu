@@ -971,6 +971,7 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
 
   CUtensorMap tmQ, tmDO, tmK, tmV;
   cudaError_t e;
+  if ((e = bind_device_context()) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmQ, a.q, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmDO, g.dout, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmK, a.k_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)

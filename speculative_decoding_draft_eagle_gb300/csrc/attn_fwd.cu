@@ -562,6 +562,7 @@ cudaError_t launch(const AttnArgs& a, void* out, float* lse, cudaStream_t s) {
   CUtensorMap tmQ, tmK, tmV, tmO;
   static thread_local SfxMaps sfx;
   cudaError_t e;
+  if ((e = bind_device_context()) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmQ, a.q, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmO, out, D, a.Q_LEN, a.B * a.H, kTile)) != cudaSuccess) return e;
   if ((e = encode_tile_map(&tmK, a.k_blocks[0], D, a.Q_LEN, a.B * a.H_kv, kTile)) != cudaSuccess)

@@ -106,4 +106,10 @@ void prof_after(cudaStream_t s);
 // Resolves cuTensorMapEncodeTiled through the runtime (no link against libcuda).
 void* tensor_map_encoder();
 
+// Makes the current device's primary context current on the calling thread.
+// The tensor-map encoder is a driver call: on a thread that has not yet made
+// a runtime call that binds the context (a fresh thread, e.g. the autograd
+// engine's), it fails.  Called before any encoding.
+cudaError_t bind_device_context();
+
 }  // namespace stt

@@ -855,6 +855,7 @@ extern "C" int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const f
                                                int64_t N, int64_t V, float* row_loss,
                                                float* loss, void* stream) {
   try {
+    (void)cudaGetLastError();  // clear an error an earlier call of this thread left behind
     if (N < 0 || V < 1 || !loss) return STT_ERR_INVALID_ARG;
     if (N > 0 && (!z || !p || !g)) return STT_ERR_INVALID_ARG;
     if (N > 0 && V > INT64_MAX / N) return STT_ERR_INVALID_ARG;

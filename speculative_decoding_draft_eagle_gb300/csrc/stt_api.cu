@@ -26,6 +26,13 @@ void* tensor_map_encoder() {
   return fn;
 }
 
+cudaError_t bind_device_context() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaSetDevice(dev);
+}
+
 namespace {
 std::atomic<uint32_t> g_inject{0};
 }  // namespace
@@ -38,7 +45,20 @@ namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int from_cuda(cudaError_t e) { return stt::status_from_cuda(e); }
+// The CUDA error the last failing call of this thread returned (read and
+// cleared by stt_last_cuda_error).
+thread_local int t_last_cuda_error = 0;
+
+int from_cuda(cudaError_t e) {
+  if (e != cudaSuccess) t_last_cuda_error = (int)e;
+  return stt::status_from_cuda(e);
+}
+
+// Every launching entry point starts here: an error that an earlier runtime
+// call of this thread left behind (someone else's) is cleared, so that the
+// check after our own launches reports only them.  A sticky error (a faulted
+// context) cannot be cleared and still fails the launches.
+inline void begin_call() { (void)cudaGetLastError(); }
 
 static_assert(STT_ERR_UNSUPPORTED == -2 && STT_ERR_CUDA == -4, "status_from_cuda codes");
 static_assert(STT_CE_BF16 == stt::kCeBf16 && STT_CE_G_PER_ELEMENT == stt::kCeGPerElement,
@@ -116,6 +136,13 @@ int stt_device_error(void* stream, uint32_t* word) {
   return (w & STT_DEVERR_WAIT_MASK) ? STT_ERR_TIMEOUT : STT_OK;
 }
 
+int stt_last_cuda_error(const char** name) {
+  const int e = t_last_cuda_error;
+  t_last_cuda_error = 0;
+  if (name) *name = cudaGetErrorName(static_cast<cudaError_t>(e));
+  return e;
+}
+
 int stt_debug_set_wait_budget(uint64_t ns) {
   cudaError_t e = stt::soft_ce_set_wait_budget(ns);
   if (e == cudaSuccess) e = stt::attn_fwd_set_wait_budget(ns);
@@ -133,6 +160,7 @@ int stt_attn_fwd(const void* q, const void* const* k_blocks, const void* const* 
                  const int32_t* T_host, int B, int H, int H_kv, int D, int Q_LEN, int k,
                  float scale, void* out, float* lse, void* stream) {
   try {
+    begin_call();
     static thread_local stt::AttnArgs a;
     int st = check_attn(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, &a);
     if (st != STT_OK) return st;
@@ -161,6 +189,7 @@ int stt_attn_bwd_ex(const void* q, const void* const* k_blocks, const void* cons
                     void* const* dk_blocks, void* const* dv_blocks, uint32_t flags,
                     void* workspace, size_t workspace_bytes, void* stream) {
   try {
+    begin_call();
     static thread_local stt::AttnArgs a;
     int st = check_attn(q, k_blocks, v_blocks, T_host, B, H, H_kv, D, Q_LEN, k, scale, &a);
     if (st != STT_OK) return st;
@@ -214,6 +243,7 @@ int soft_ce_fwd_bwd_inplace(float* z, const float* p, const float* g, int64_t N,
                             float* row_loss, float* loss, void* workspace,
                             size_t workspace_bytes, void* stream) {
   try {
+    begin_call();
     if (N < 0 || V < 1 || !loss) return STT_ERR_INVALID_ARG;
     if (N > 0 && (!z || !p || !g)) return STT_ERR_INVALID_ARG;
     if (N > 0 && V > INT64_MAX / N) return STT_ERR_INVALID_ARG;
@@ -235,6 +265,7 @@ int soft_ce_fwd_bwd_inplace_ex(void* z, const void* p, const float* g, int64_t N
                                uint32_t flags, float* row_loss, float* loss, void* workspace,
                                size_t workspace_bytes, void* stream) {
   try {
+    begin_call();
     if (flags & ~(uint32_t)(STT_CE_BF16 | STT_CE_G_PER_ELEMENT)) return STT_ERR_INVALID_ARG;
     if (flags == 0)
       return soft_ce_fwd_bwd_inplace(static_cast<float*>(z), static_cast<const float*>(p), g, N,

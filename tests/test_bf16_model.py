@@ -5,8 +5,8 @@ shapes (no GPU needed).
 fp64 with the roundings of the GPU path: O stored in bf16 feeds
 Delta = rowsum(dO * O), and in the causal block P and dS enter the tensor
 cores as bf16.  Pins: with the roundings switched off it is the oracle's
-backward; with them on, its error follows bf16's unit roundoff (2^-9 relative
-per rounding), and on the degenerate shapes (many padded rows sharing one or
+backward; with them on, its error follows bf16's unit roundoff (2^-8 relative
+per rounding: 8 significant bits), and on the degenerate shapes (many padded rows sharing one or
 two keys, |dK| ~ 10) it predicts errors above the flat 2e-2, which is why the
 GPU test bounds those tensors by twice the predicted error instead."""
 
@@ -50,7 +50,7 @@ def test_rounding_error_is_bf16_sized_and_flags_the_degenerate_shapes():
             err = float(np.abs(e - r).max())
             nref = float(np.linalg.norm(r))
             rel = float(np.linalg.norm(e - r)) / nref if nref > 0 else 0.0
-            # each rounding is at most 2^-9 relative; sums of many such terms
+            # each rounding is at most 2^-8 relative; sums of many such terms
             # stay well below a few units of 2^-9 of the largest entry
             assert err <= 2.0 ** -6 * max(1e-30, float(np.abs(r).max()))
             assert rel <= 2.0 ** -6
