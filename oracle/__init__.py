@@ -20,7 +20,9 @@ attention  masked softmax attention over the concatenated TTT KV blocks,
            forward and backward, written from the definition.
 soft_ce    the masked soft-target softmax cross-entropy and its in-place
            gradient (SpecForge review, §三 "内存高效梯度计算", §四
-           "掩码 Softmax 损失" / "原地反向传播").
+           "掩码 Softmax 损失" / "原地反向传播"), per-row or per-element g.
+verify     speculative-decoding verification by rejection sampling (the
+           "FlashSpec" practice page, §3.4 "验证器的具体实现").
 
 Readings of the page where it is silent:
   * kv indexes the concatenation of k+1 blocks, each Q_LEN long; block 0 is
@@ -36,6 +38,6 @@ Readings of the page where it is silent:
     loss).                                -> convention, parity unpinned
 """
 
-from . import mask, attention, soft_ce  # noqa: F401
+from . import mask, attention, soft_ce, verify  # noqa: F401
 
-__all__ = ["mask", "attention", "soft_ce"]
+__all__ = ["mask", "attention", "soft_ce", "verify"]

@@ -1,0 +1,85 @@
+"""Speculative-decoding verification by rejection sampling (oracle; test
+infrastructure).
+
+Source: the "FlashSpec" practice page, §3.4 "验证器的具体实现" (how the
+verifier decides to accept or reject).  For each sequence b, the draft
+proposed tokens x_0 .. x_{gamma-1}; at position i the draft's distribution is
+p_d[b, i, :] and the target model's is p_t[b, i, :].  Walking the positions
+in order:
+
+    accept x_i   with probability min(1, p_t[x_i] / p_d[x_i]);
+    otherwise    sample one token from norm(max(0, p_t - p_d)) at that
+                 position, append it, and stop.
+
+Every accepted token is appended; the page's verifier draws nothing more when
+all gamma tokens are accepted.  The page states the purpose: the tokens that
+come out follow the target model's distribution exactly.
+
+Readings where the page is silent:
+  * The random numbers are inputs: u_accept[b, i] in [0, 1) for the test at
+    position i, u_sample[b] in [0, 1) for the one resampling draw.  "With
+    probability a" is u < a.
+  * The test u < min(1, p_t / p_d) is evaluated as u * p_d < p_t in float64
+    (exact for float32 inputs, and the same for p_d > 0); a draft token with
+    p_d = 0 is accepted iff p_t > 0.
+  * Sampling from norm(r), r_v = max(0, p_t[v] - p_d[v]) (float64), with one
+    uniform u: the smallest y with r_0 + ... + r_y > u * sum(r) (inverse CDF).
+  * If sum(r) = 0 the draw is taken from p_t itself by the same rule
+    (convention: it arises only when p_t <= p_d everywhere).
+  * Output per sequence: the number of accepted draft tokens n_acc, and
+    tokens[b, :] = x_0 .. x_{n_acc-1}, then the resampled token if
+    n_acc < gamma, then -1.
+"""
+
+import numpy as np
+
+
+def inverse_cdf(weights, u):
+    """Smallest index y with weights[0] + ... + weights[y] > u * sum(weights)
+    (plain sequential float64 sums); the last positive index if rounding puts
+    the threshold past the total."""
+    w = np.asarray(weights, dtype=np.float64)
+    total = float(w.sum())
+    thresh = float(u) * total
+    acc = 0.0
+    last = -1
+    for y in range(len(w)):
+        if w[y] > 0.0:
+            last = y
+        acc += float(w[y])
+        if acc > thresh:
+            return y
+    return last
+
+
+def verify_row(p_t, p_d, tokens, u_accept, u_sample):
+    """One sequence: p_t, p_d [gamma, V]; tokens, u_accept [gamma]; u_sample scalar.
+    Returns (n_acc, out [gamma] int64)."""
+    p_t = np.asarray(p_t, dtype=np.float64)
+    p_d = np.asarray(p_d, dtype=np.float64)
+    gamma = len(tokens)
+    out = np.full(gamma, -1, dtype=np.int64)
+    for i in range(gamma):
+        x = int(tokens[i])
+        pt, pd = float(p_t[i, x]), float(p_d[i, x])
+        accept = (float(u_accept[i]) * pd < pt) if pd > 0.0 else (pt > 0.0)
+        if accept:
+            out[i] = x
+            continue
+        r = np.maximum(0.0, p_t[i] - p_d[i])
+        if float(r.sum()) == 0.0:
+            r = p_t[i]
+        out[i] = inverse_cdf(r, u_sample)
+        return i, out
+    return gamma, out
+
+
+def verify(p_t, p_d, tokens, u_accept, u_sample):
+    """All sequences: p_t, p_d [B, gamma, V]; tokens, u_accept [B, gamma];
+    u_sample [B].  Returns (n_acc [B] int64, out [B, gamma] int64)."""
+    B = len(tokens)
+    n_acc = np.zeros(B, dtype=np.int64)
+    out = np.zeros((B, len(tokens[0])), dtype=np.int64)
+    for b in range(B):
+        n_acc[b], out[b] = verify_row(p_t[b], p_d[b], tokens[b], u_accept[b], u_sample[b])
+    return n_acc, out
