@@ -290,6 +290,37 @@ STT_API int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const floa
                                             void* stream);
 
 /* --------------------------------------------------------------------------
+ * Speculative-decoding verification by rejection sampling (the "FlashSpec"
+ * practice page, §3.4 "验证器的具体实现").  For each sequence b the draft's
+ * tokens x_0..x_{gamma-1} are tested in order: x_i is accepted with
+ * probability min(1, p_t[x_i] / p_d[x_i]), evaluated as
+ * u_accept[b, i] * p_d < p_t in fp64 (a token with p_d = 0 is accepted iff
+ * p_t > 0; a token outside [0, V) never).  At the first rejection one token
+ * is drawn from norm(max(0, p_t - p_d)) at that position -- the smallest y
+ * whose running residual sum (fp64) exceeds u_sample[b] times the total, or
+ * from p_t itself if the residual is all zero -- and the sequence stops.
+ * Nothing is drawn when every token is accepted.
+ *
+ *  p_target   fp32 [B, gamma, V]: the target model's distribution at each
+ *             draft position.
+ *  p_draft    fp32 [B, gamma, V]: the draft's distribution there.
+ *  draft_tokens int32 [B, gamma].
+ *  u_accept   fp32 [B, gamma], uniform in [0, 1): the acceptance draws.
+ *  u_sample   fp32 [B], uniform in [0, 1): the resampling draw.
+ *  B >= 0 (0 does nothing), 1 <= gamma <= STT_VERIFY_MAX_GAMMA, V >= 1.
+ *  n_accepted int32 [B]: accepted draft tokens per sequence.
+ *  out_tokens int32 [B, gamma]: the accepted tokens, then the drawn token if
+ *             n_accepted < gamma, then -1.
+ * All pointers device, 4-byte aligned (rows that are 16-byte aligned with
+ * V % 4 == 0 are read with 16-byte loads).  The random numbers are inputs,
+ * so a call is deterministic.
+ * ------------------------------------------------------------------------ */
+#define STT_VERIFY_MAX_GAMMA 32
+STT_API int stt_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
+                       const float* u_accept, const float* u_sample, int B, int gamma, int64_t V,
+                       int32_t* n_accepted, int32_t* out_tokens, void* stream);
+
+/* --------------------------------------------------------------------------
  * Per-launch timing (measurement support; no counterpart on the pages).
  * stt_profile_start(capacity) makes every subsequent kernel launch of the
  * library (from any thread) record a CUDA event pair around itself on its
@@ -314,6 +345,7 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_KERNEL_ATTN_BWD_CAUSAL 5
 #define STT_KERNEL_ATTN_BWD_CAST 6
 #define STT_KERNEL_SOFT_CE_VARIANT 7
+#define STT_KERNEL_VERIFY 8
 
 /* Device error-word bits: sites of bounded waits that gave up, and blocks
  * whose dynamic shared memory did not have the 1024-byte alignment the

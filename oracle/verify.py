@@ -26,6 +26,9 @@ Readings where the page is silent:
     uniform u: the smallest y with r_0 + ... + r_y > u * sum(r) (inverse CDF).
   * If sum(r) = 0 the draw is taken from p_t itself by the same rule
     (convention: it arises only when p_t <= p_d everywhere).
+  * A draft token outside [0, V) has probability 0 under both models, so it
+    is never accepted (convention for invalid input).
+  * A target row that is all zero leaves nothing to draw: the token is -1.
   * Output per sequence: the number of accepted draft tokens n_acc, and
     tokens[b, :] = x_0 .. x_{n_acc-1}, then the resampled token if
     n_acc < gamma, then -1.
@@ -59,9 +62,11 @@ def verify_row(p_t, p_d, tokens, u_accept, u_sample):
     p_d = np.asarray(p_d, dtype=np.float64)
     gamma = len(tokens)
     out = np.full(gamma, -1, dtype=np.int64)
+    V = p_t.shape[1]
     for i in range(gamma):
         x = int(tokens[i])
-        pt, pd = float(p_t[i, x]), float(p_d[i, x])
+        # a token outside the vocabulary has no probability under either model
+        pt, pd = (float(p_t[i, x]), float(p_d[i, x])) if 0 <= x < V else (0.0, 0.0)
         accept = (float(u_accept[i]) * pd < pt) if pd > 0.0 else (pt > 0.0)
         if accept:
             out[i] = x

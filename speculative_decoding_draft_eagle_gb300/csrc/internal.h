@@ -44,6 +44,11 @@ cudaError_t soft_ce_variant_launch(const CeVariantPlan& plan, uint32_t flags, vo
                                    const void* p, const float* g, int64_t N, int64_t V,
                                    float* row_loss, float* loss, float* wl, cudaStream_t s);
 
+// ---------------------------------------------------------- verification --
+cudaError_t verify_launch(const float* p_t, const float* p_d, const int32_t* tokens,
+                          const float* u_accept, const float* u_sample, int B, int gamma,
+                          int64_t V, int32_t* n_acc, int32_t* out, cudaStream_t s);
+
 // ----------------------------------------------------------- attention ----
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxBlocks = 32;

@@ -100,6 +100,7 @@ const char* stt_kernel_name(int kernel_id) {
     case STT_KERNEL_ATTN_BWD_CAUSAL: return "attn_bwd_causal";
     case STT_KERNEL_ATTN_BWD_CAST: return "attn_bwd_cast";
     case STT_KERNEL_SOFT_CE_VARIANT: return "soft_ce_variant";
+    case STT_KERNEL_VERIFY: return "verify";
     default: return "unknown";
   }
 }

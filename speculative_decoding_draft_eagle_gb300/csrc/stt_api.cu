@@ -286,4 +286,32 @@ int soft_ce_fwd_bwd_inplace_ex(void* z, const void* p, const float* g, int64_t N
   }
 }
 
+int stt_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
+               const float* u_accept, const float* u_sample, int B, int gamma, int64_t V,
+               int32_t* n_accepted, int32_t* out_tokens, void* stream) {
+  try {
+    begin_call();
+    if (B < 0 || gamma < 1 || gamma > STT_VERIFY_MAX_GAMMA || V < 1) return STT_ERR_INVALID_ARG;
+    if (B == 0) return STT_OK;
+    if (!p_target || !p_draft || !draft_tokens || !u_accept || !u_sample || !n_accepted ||
+        !out_tokens)
+      return STT_ERR_INVALID_ARG;
+    if ((long long)B * gamma > INT64_MAX / V) return STT_ERR_INVALID_ARG;
+    if (V > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p_target) |
+                        reinterpret_cast<uintptr_t>(p_draft) |
+                        reinterpret_cast<uintptr_t>(draft_tokens) |
+                        reinterpret_cast<uintptr_t>(u_accept) |
+                        reinterpret_cast<uintptr_t>(u_sample) |
+                        reinterpret_cast<uintptr_t>(n_accepted) |
+                        reinterpret_cast<uintptr_t>(out_tokens);
+    if (a & 3u) return STT_ERR_MISALIGNED;
+    return from_cuda(stt::verify_launch(p_target, p_draft, draft_tokens, u_accept, u_sample, B,
+                                        gamma, V, n_accepted, out_tokens,
+                                        static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
 }  // extern "C"

@@ -25,6 +25,7 @@ __all__ = [
     "soft_ce_fwd_bwd_inplace_ex",
     "soft_ce_fwd_bwd_inplace_noalloc",
     "soft_ce_workspace_size",
+    "stt_verify",
     "stt_device_error",
     "stt_debug_set_wait_budget",
     "stt_debug_inject",
@@ -292,6 +293,35 @@ def soft_ce_fwd_bwd_inplace_noalloc(z: torch.Tensor, p: torch.Tensor, g: torch.T
 
 
 STT_ERR_TIMEOUT = -5
+
+
+def stt_verify(p_target: torch.Tensor, p_draft: torch.Tensor, draft_tokens: torch.Tensor,
+               u_accept: torch.Tensor, u_sample: torch.Tensor,
+               n_accepted: Optional[torch.Tensor] = None,
+               out_tokens: Optional[torch.Tensor] = None, stream=None):
+    """Rejection-sampling verification of draft tokens.  p_target, p_draft fp32
+    [B, gamma, V]; draft_tokens int32 [B, gamma]; u_accept fp32 [B, gamma];
+    u_sample fp32 [B].  Returns (n_accepted int32 [B], out_tokens int32 [B, gamma])."""
+    if p_target.dim() != 3:
+        raise ValueError("p_target must be [B, gamma, V]")
+    B, gamma, V = p_target.shape
+    _need(p_target, "p_target", torch.float32)
+    _need(p_draft, "p_draft", torch.float32, (B, gamma, V))
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, gamma))
+    _need(u_accept, "u_accept", torch.float32, (B, gamma))
+    _need(u_sample, "u_sample", torch.float32, (B,))
+    dev = p_target.device
+    if n_accepted is None:
+        n_accepted = torch.empty(B, device=dev, dtype=torch.int32)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma), device=dev, dtype=torch.int32)
+    _need(n_accepted, "n_accepted", torch.int32, (B,))
+    _need(out_tokens, "out_tokens", torch.int32, (B, gamma))
+    st = lib().stt_verify(_ptr(p_target), _ptr(p_draft), _ptr(draft_tokens), _ptr(u_accept),
+                          _ptr(u_sample), B, gamma, V, _ptr(n_accepted), _ptr(out_tokens),
+                          _stream(stream))
+    check("stt_verify", st)
+    return n_accepted, out_tokens
 
 
 def stt_device_error(stream=None) -> int:

@@ -164,3 +164,39 @@ def soft_ce_inputs(sc: SoftCEShape, device, seed: int, T: Sequence[int] = None,
         keep = torch.where(pos < lim, keep, torch.zeros_like(keep))
     g = (keep / N).to(torch.float32).to(device)
     return z, p, g
+
+
+@dataclasses.dataclass(frozen=True)
+class VerifyShape:
+    """Rejection-sampling verification: B sequences, gamma draft tokens each,
+    vocabulary V.  The target's distribution is softmax(N(0, sigma^2) / temp);
+    the draft's is softmax((target logits + N(0, noise^2)) / temp), so the two
+    agree roughly as a trained draft does; the draft tokens are drawn from the
+    draft's distribution."""
+    B: int
+    gamma: int
+    V: int
+    sigma: float = 2.0
+    noise: float = 0.5
+    temp: float = 0.8
+
+
+# B 64 sequences, 5 draft tokens each (num_speculative_tokens = 5 of the
+# FlashSpec practice page), Qwen-sized vocabulary.
+VERIFY = VerifyShape(B=64, gamma=5, V=151936)
+
+
+def verify_inputs(vs: VerifyShape, device, seed: int):
+    """p_target, p_draft fp32 [B, gamma, V]; draft_tokens int32 [B, gamma];
+    u_accept fp32 [B, gamma] and u_sample fp32 [B], uniform in [0, 1)."""
+    shape = (vs.B, vs.gamma, vs.V)
+    lt = torch.randn(shape, generator=_gen(device, seed, 60), device=device) * vs.sigma
+    p_t = torch.softmax(lt / vs.temp, dim=-1)
+    ld = lt + torch.randn(shape, generator=_gen(device, seed, 61), device=device) * vs.noise
+    p_d = torch.softmax(ld / vs.temp, dim=-1)
+    del lt, ld
+    toks = torch.multinomial(p_d.reshape(-1, vs.V), 1, generator=_gen(device, seed, 62))
+    toks = toks.reshape(vs.B, vs.gamma).to(torch.int32)
+    u_acc = torch.rand((vs.B, vs.gamma), generator=_gen(device, seed, 63), device=device)
+    u_smp = torch.rand((vs.B,), generator=_gen(device, seed, 64), device=device)
+    return p_t, p_d, toks, u_acc, u_smp

@@ -130,3 +130,14 @@ def test_soft_ce_ex_rejects_bad_arguments(L):
     assert f(good, good, good, -1, 10, 0x1, None, good, good, 1 << 20, None) == -1
     assert f(good, good, good, 4, 10, 0x1, None, good, None, 0, None) == -6
     assert f(good, good, good, 4, 10_000_000, 0x2, None, good, good, 1 << 20, None) == -2
+
+
+def test_verify_rejects_bad_arguments(L):
+    good = 0x1000
+    f = L.stt_verify
+    assert f(good, good, good, good, good, 0, 5, 100, good, good, None) == 0   # B = 0: nothing to do
+    assert f(good, good, good, good, good, 2, 0, 100, good, good, None) == -1
+    assert f(good, good, good, good, good, 2, 33, 100, good, good, None) == -1
+    assert f(good, good, good, good, good, 2, 5, 0, good, good, None) == -1
+    assert f(None, good, good, good, good, 2, 5, 100, good, good, None) == -1
+    assert f(good + 2, good, good, good, good, 2, 5, 100, good, good, None) == -3
