@@ -21,6 +21,8 @@ attention  masked softmax attention over the concatenated TTT KV blocks,
 soft_ce    the masked soft-target softmax cross-entropy and its in-place
            gradient (SpecForge review, §三 "内存高效梯度计算", §四
            "掩码 Softmax 损失" / "原地反向传播"), per-row or per-element g.
+lm_head    the draft's LM head z = h W^T followed by the soft-CE: loss and
+           the gradients of h and W.
 verify     speculative-decoding verification by rejection sampling (the
            "FlashSpec" practice page, §3.4 "验证器的具体实现").
 
@@ -38,6 +40,6 @@ Readings of the page where it is silent:
     loss).                                -> convention, parity unpinned
 """
 
-from . import mask, attention, soft_ce, verify  # noqa: F401
+from . import mask, attention, soft_ce, lm_head, verify  # noqa: F401
 
-__all__ = ["mask", "attention", "soft_ce", "verify"]
+__all__ = ["mask", "attention", "soft_ce", "lm_head", "verify"]
