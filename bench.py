@@ -63,6 +63,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true")
     ap.add_argument("--other-steps", type=int, default=5)
+    ap.add_argument("--no-extras", action="store_true")
     a = ap.parse_args()
     if a.warmup < 0 or a.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -397,6 +398,11 @@ def run_ours(a):
             del ob
             torch.cuda.empty_cache()
 
+    extras = None
+    if not a.no_extras:
+        extras = measure_extras(dev, stream, pk, ops)
+        assert ops.stt_device_error(stream) == 0
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(total_ms / a.steps, 4),
@@ -421,12 +427,124 @@ def run_ours(a):
         "e2e": e2e,
         "clocks": r["clocks"],
         "other_workloads": others or None,
+        "extras": extras,
     }
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(name)
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
+
+
+def _time_calls(fn, n, warmup, stream, before=None):
+    """Device time (ms) of n calls of fn(i) after `warmup` untimed ones; before(i),
+    if given, runs outside the timed events (input refill, L2 flush)."""
+    for i in range(warmup):
+        if before:
+            before(i)
+        fn(i)
+    torch.cuda.synchronize()
+    tot = 0.0
+    for i in range(n):
+        if before:
+            before(warmup + i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn(warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    return tot
+
+
+def measure_extras(dev, stream, pk, ops, steps=10, warmup=3):
+    """The rows beyond the attention + soft-CE step, each timed alone with CUDA
+    events (inputs larger than L2, or L2 flushed between calls)."""
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+
+    # fused draft LM head + soft-CE (Llama-8B draft shape)
+    ls = wl.LM_HEAD
+    h, W, p, g = wl.lm_head_inputs(ls, dev, 1002)
+    dh = torch.empty((ls.N, ls.Hd), device=dev)
+    dW = torch.empty((ls.V, ls.Hd), device=dev)
+    rl = torch.empty(ls.N, device=dev)
+    lo = torch.empty(1, device=dev)
+    ws = torch.empty(int(ops.lib().stt_lm_head_ce_workspace_size(ls.N, ls.Hd, ls.V)),
+                     device=dev, dtype=torch.uint8)
+    ms = _time_calls(lambda i: ops.stt_lm_head_ce(h, W, p, g, dh=dh, dW=dW, row_loss=rl, loss=lo,
+                                                  workspace=ws, stream=stream),
+                     steps, warmup, stream) / steps
+    fl = 4 * 2.0 * ls.N * ls.V * ls.Hd  # z (twice: statistics, then per chunk), dh, dW
+    ach = fl / (ms * 1e-3) / 1e12
+    out["lm_head_ce"] = {"workload": f"N {ls.N}, Hd {ls.Hd}, V {ls.V} (Llama-3.1-8B draft head)",
+                         "ms_per_call": round(ms, 4), "achieved": round(ach, 1), "unit": "TFLOP/s",
+                         "flops_counted": "4 GEMMs of 2 N V Hd: z for the statistics, z again "
+                                          "per chunk for dz, dh = dz W, dW = dz^T h",
+                         "peak": pk["bf16"], "frac": round(ach / pk["bf16"], 4),
+                         "logits_bytes_avoided": int(ls.N * ls.V * 4)}
+    del h, W, p, g, dh, dW, ws
+    torch.cuda.empty_cache()
+
+    # rejection-sampling verification
+    vs = wl.VERIFY
+    p_t, p_d, toks, ua, us = wl.verify_inputs(vs, dev, 1006)
+    n_acc = torch.empty(vs.B, device=dev, dtype=torch.int32)
+    o_t = torch.empty((vs.B, vs.gamma), device=dev, dtype=torch.int32)
+    ops.stt_verify(p_t, p_d, toks, ua, us, n_accepted=n_acc, out_tokens=o_t, stream=stream)
+    torch.cuda.synchronize()
+    na = n_acc.cpu()
+    rejected = int((na < vs.gamma).sum())
+    tested = int(torch.clamp(na + 1, max=vs.gamma).sum())
+    vbytes = tested * 8 + rejected * 2 * vs.V * 4 + vs.B * (vs.gamma * 12 + 8)
+    ms = _time_calls(lambda i: ops.stt_verify(p_t, p_d, toks, ua, us, n_accepted=n_acc,
+                                              out_tokens=o_t, stream=stream),
+                     steps, warmup, stream, before=lambda i: flush.fill_(i & 255)) / steps
+    out["verify"] = {"workload": f"B {vs.B}, gamma {vs.gamma}, V {vs.V}; {rejected} sequences "
+                                 f"with a rejection, mean accepted {float(na.float().mean()):.2f}",
+                     "ms_per_call": round(ms, 5), "sequences_per_s": round(vs.B / (ms * 1e-3)),
+                     "achieved": round(vbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                     "algorithmic_bytes": vbytes, "peak": pk["hbm"],
+                     "frac": round(vbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4),
+                     "l2": "flushed (256 MB write) before every call"}
+    del p_t, p_d, toks, ua, us
+    torch.cuda.empty_cache()
+
+    # soft-CE variants on the Llama-8B soft-CE shape
+    sc = wl.WORKLOADS["llama8b"].soft_ce
+    z0, pp, g = wl.soft_ce_inputs(sc, dev, 1002)
+    gr = torch.Generator(device=dev).manual_seed(5)
+    G = (torch.rand(z0.shape, generator=gr, device=dev) < 0.8).float() / sc.N
+    nz = int((g != 0).sum())
+    for tag, zdt, gel in (("bf16_z_p", torch.bfloat16, False), ("per_element_g", torch.float32, True)):
+        zb = z0.to(zdt)
+        pb = pp.to(zdt)
+        gg = G if gel else g
+        R = 4
+        zs = [torch.empty_like(zb) for _ in range(R)]
+        wsc = torch.empty(ops.soft_ce_workspace_size(sc.N, sc.V), device=dev, dtype=torch.uint8)
+        lo = torch.empty(1, device=dev)
+        rl = torch.empty(sc.N, device=dev)
+
+        def refill(i, zs=zs, zb=zb):
+            zs[i % R].copy_(zb)
+
+        ms = _time_calls(lambda i, zs=zs, pb=pb, gg=gg: ops.soft_ce_fwd_bwd_inplace_ex(
+            zs[i % R], pb, gg, row_loss=rl, loss=lo, workspace=wsc, stream=stream),
+            steps, warmup, stream, before=refill) / steps
+        es = zb.element_size()
+        if gel:
+            vb = sc.N * sc.V * (3 * es + 4) + 8 * sc.N
+        else:
+            vb = nz * sc.V * 3 * es + (sc.N - nz) * sc.V * es + 8 * sc.N
+        ach = vb / (ms * 1e-3) / 1e9
+        out[f"soft_ce_{tag}"] = {"workload": f"N {sc.N}, V {sc.V}", "ms_per_call": round(ms, 4),
+                                 "achieved": round(ach, 1), "unit": "GB/s",
+                                 "peak": pk["hbm"], "frac": round(ach / pk["hbm"], 4)}
+        del zs, zb, pb
+    del z0, pp, g, G, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(a, wb, dev, stream, flops, world):

@@ -290,6 +290,36 @@ STT_API int soft_ce_fwd_bwd_inplace_noalloc(float* z, const float* p, const floa
                                             void* stream);
 
 /* --------------------------------------------------------------------------
+ * The draft's LM head fused with the soft-CE, chunked over the vocabulary
+ * (SpecForge review, §三 "内存高效梯度计算": the logits are the activation the
+ * in-place gradient saves memory on; §四 "原地反向传播").  With hidden states
+ * h, head weights W, targets p and per-row upstream gradients g:
+ *     z = h W^T,  L = sum_r g_r l_r (l_r and dL/dz as soft_ce_fwd_bwd_inplace),
+ *     dh = (dL/dz) W,  dW = (dL/dz)^T h.
+ * The logits are never stored: a tensor-core pass computes per-row softmax
+ * statistics from z tile by tile, and a second pass recomputes z one
+ * vocabulary chunk at a time and turns it into dL/dz (bf16, in the
+ * workspace), which feeds dh and dW at once.
+ *
+ *  h        bf16 [N, Hd] row-major.      W  bf16 [V, Hd] row-major.
+ *  p        fp32 [N, V].                 g  fp32 [N].
+ *  N >= 0; Hd and V multiples of 8 (STT_ERR_UNSUPPORTED otherwise), >= 8.
+ *  dh       fp32 [N, Hd], OVERWRITTEN with dL/dh.
+ *  dW       fp32 [V, Hd], OVERWRITTEN with dL/dW.
+ *  row_loss fp32 [N] or NULL: l_r (0 for rows with g_r = 0).
+ *  loss     fp32 scalar (device): L, summed in a fixed order.
+ *  workspace at least stt_lm_head_ce_workspace_size(N, Hd, V) bytes,
+ *           256-byte aligned; h, W, p, dh, dW 16-byte aligned.
+ * dL/dz enters the two gradient products rounded to bf16 (as the operands of
+ * any bf16 training step); sums are fp32.
+ * ------------------------------------------------------------------------ */
+STT_API size_t stt_lm_head_ce_workspace_size(int64_t N, int64_t Hd, int64_t V);
+STT_API int stt_lm_head_ce(const void* h, const void* W, const float* p, const float* g,
+                           int64_t N, int64_t Hd, int64_t V, float* dh, float* dW,
+                           float* row_loss, float* loss, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * Speculative-decoding verification by rejection sampling (the "FlashSpec"
  * practice page, §3.4 "验证器的具体实现").  For each sequence b the draft's
  * tokens x_0..x_{gamma-1} are tested in order: x_i is accepted with
@@ -346,6 +376,7 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_KERNEL_ATTN_BWD_CAST 6
 #define STT_KERNEL_SOFT_CE_VARIANT 7
 #define STT_KERNEL_VERIFY 8
+#define STT_KERNEL_LM_HEAD_CE 9
 
 /* Device error-word bits: sites of bounded waits that gave up, and blocks
  * whose dynamic shared memory did not have the 1024-byte alignment the
@@ -354,7 +385,9 @@ STT_API const char* stt_kernel_name(int kernel_id);
 #define STT_DEVERR_BWD_WAIT 0x2u
 #define STT_DEVERR_CE_WAIT 0x4u
 #define STT_DEVERR_SMEM_ALIGN 0x8u
-#define STT_DEVERR_WAIT_MASK (STT_DEVERR_FWD_WAIT | STT_DEVERR_BWD_WAIT | STT_DEVERR_CE_WAIT)
+#define STT_DEVERR_LM_WAIT 0x10u
+#define STT_DEVERR_WAIT_MASK \
+  (STT_DEVERR_FWD_WAIT | STT_DEVERR_BWD_WAIT | STT_DEVERR_CE_WAIT | STT_DEVERR_LM_WAIT)
 
 #ifdef __cplusplus
 }

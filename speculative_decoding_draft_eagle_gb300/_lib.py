@@ -41,6 +41,8 @@ EXPORTS = (
     "soft_ce_fwd_bwd_inplace_ex",
     "soft_ce_fwd_bwd_inplace_noalloc",
     "stt_verify",
+    "stt_lm_head_ce_workspace_size",
+    "stt_lm_head_ce",
     "stt_profile_start",
     "stt_profile_stop",
     "stt_kernel_name",
@@ -92,6 +94,10 @@ def _declare(L):
     L.soft_ce_fwd_bwd_inplace.restype = i32
     L.soft_ce_fwd_bwd_inplace_ex.argtypes = [vp, vp, vp, i64, i64, c.c_uint32, vp, vp, vp, sz, vp]
     L.soft_ce_fwd_bwd_inplace_ex.restype = i32
+    L.stt_lm_head_ce_workspace_size.argtypes = [i64, i64, i64]
+    L.stt_lm_head_ce_workspace_size.restype = sz
+    L.stt_lm_head_ce.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, sz, vp]
+    L.stt_lm_head_ce.restype = i32
     L.stt_verify.argtypes = [vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp]
     L.stt_verify.restype = i32
     L.soft_ce_fwd_bwd_inplace_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp]

@@ -71,32 +71,6 @@ inline cudaError_t encode_f32_map(CUtensorMap* map, const void* base, int D, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Warp-uniform bounded wait: every lane waits, the warp agrees on success.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t site) {
-  const bool ok = mbar_wait(bar, parity, site);
-  return __all_sync(0xffffffffu, ok) != 0;
-}
-
-// One arrival per warp on `bar` (an mbarrier counting warps): the warp's lanes
-// first meet at __syncwarp, which orders their prior shared-memory and (after
-// their own tcgen05 fences) tensor-memory accesses before lane 0's release
-// arrive.  Every lane of the warp must call it.
-__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
-// Bounded barrier among the warps counted by `bar` (an mbarrier initialised
-// with that many warps).  Unlike a named hardware barrier it cannot deadlock
-// when some warp gave up on an earlier bounded wait: the others time out too.
-// `uses` counts this thread's completed phases (same sequence in every thread).
-__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& uses, uint32_t site) {
-  warp_arrive(bar);
-  const bool ok = warp_wait(bar, uses & 1u, site);
-  ++uses;
-  return ok;
-}
-
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -44,6 +44,14 @@ cudaError_t soft_ce_variant_launch(const CeVariantPlan& plan, uint32_t flags, vo
                                    const void* p, const float* g, int64_t N, int64_t V,
                                    float* row_loss, float* loss, float* wl, cudaStream_t s);
 
+// ------------------------------------------------------- LM head + soft-CE --
+size_t lm_head_ce_workspace(int64_t N, int64_t V);
+cudaError_t lm_head_ce_launch(const void* h, const void* W, const float* p, const float* g,
+                              int64_t N, int64_t Hd, int64_t V, float* dh, float* dW,
+                              float* row_loss, float* loss, void* workspace, cudaStream_t s);
+cudaError_t lm_head_error_word(uint32_t* w);
+cudaError_t lm_head_set_wait_budget(uint64_t ns);
+
 // ---------------------------------------------------------- verification --
 cudaError_t verify_launch(const float* p_t, const float* p_d, const int32_t* tokens,
                           const float* u_accept, const float* u_sample, int B, int gamma,

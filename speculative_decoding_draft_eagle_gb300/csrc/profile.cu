@@ -101,6 +101,7 @@ const char* stt_kernel_name(int kernel_id) {
     case STT_KERNEL_ATTN_BWD_CAST: return "attn_bwd_cast";
     case STT_KERNEL_SOFT_CE_VARIANT: return "soft_ce_variant";
     case STT_KERNEL_VERIFY: return "verify";
+    case STT_KERNEL_LM_HEAD_CE: return "lm_head_ce";
     default: return "unknown";
   }
 }

@@ -132,6 +132,8 @@ int stt_device_error(void* stream, uint32_t* word) {
   w |= part;
   if (stt::attn_bwd_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
   w |= part;
+  if (stt::lm_head_error_word(&part) != cudaSuccess) return STT_ERR_CUDA;
+  w |= part;
   *word = w;
   return (w & STT_DEVERR_WAIT_MASK) ? STT_ERR_TIMEOUT : STT_OK;
 }
@@ -147,6 +149,7 @@ int stt_debug_set_wait_budget(uint64_t ns) {
   cudaError_t e = stt::soft_ce_set_wait_budget(ns);
   if (e == cudaSuccess) e = stt::attn_fwd_set_wait_budget(ns);
   if (e == cudaSuccess) e = stt::attn_bwd_set_wait_budget(ns);
+  if (e == cudaSuccess) e = stt::lm_head_set_wait_budget(ns);
   return from_cuda(e);
 }
 
@@ -281,6 +284,34 @@ int soft_ce_fwd_bwd_inplace_ex(void* z, const void* p, const float* g, int64_t N
     return from_cuda(stt::soft_ce_variant_launch(plan, flags, z, p, g, N, V, row_loss, loss,
                                                  static_cast<float*>(workspace),
                                                  static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return STT_ERR_CUDA;
+  }
+}
+
+size_t stt_lm_head_ce_workspace_size(int64_t N, int64_t Hd, int64_t V) {
+  (void)Hd;
+  if (N < 0 || V < 1) return 16;
+  return stt::lm_head_ce_workspace(N, V);
+}
+
+int stt_lm_head_ce(const void* h, const void* W, const float* p, const float* g, int64_t N,
+                   int64_t Hd, int64_t V, float* dh, float* dW, float* row_loss, float* loss,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    begin_call();
+    if (N < 0 || Hd < 8 || V < 8 || !loss) return STT_ERR_INVALID_ARG;
+    if (Hd % 8 != 0 || V % 8 != 0) return STT_ERR_UNSUPPORTED;
+    if (N > 0x7fffffffLL || Hd > 0x7fffffffLL || V > 0x7fffffffLL) return STT_ERR_UNSUPPORTED;
+    if (N > 0 && (!h || !W || !p || !g || !dh || !dW)) return STT_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < stt::lm_head_ce_workspace(N, V)) return STT_ERR_WORKSPACE;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(W) |
+                        reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(dh) |
+                        reinterpret_cast<uintptr_t>(dW);
+    if ((a & 15u) != 0 || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return STT_ERR_MISALIGNED;
+    return from_cuda(stt::lm_head_ce_launch(h, W, p, g, N, Hd, V, dh, dW, row_loss, loss,
+                                            workspace, static_cast<cudaStream_t>(stream)));
   } catch (...) {
     return STT_ERR_CUDA;
   }

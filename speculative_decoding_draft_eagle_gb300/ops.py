@@ -26,6 +26,7 @@ __all__ = [
     "soft_ce_fwd_bwd_inplace_noalloc",
     "soft_ce_workspace_size",
     "stt_verify",
+    "stt_lm_head_ce",
     "stt_device_error",
     "stt_debug_set_wait_budget",
     "stt_debug_inject",
@@ -293,6 +294,44 @@ def soft_ce_fwd_bwd_inplace_noalloc(z: torch.Tensor, p: torch.Tensor, g: torch.T
 
 
 STT_ERR_TIMEOUT = -5
+
+
+def stt_lm_head_ce(h: torch.Tensor, W: torch.Tensor, p: torch.Tensor, g: torch.Tensor,
+                   dh: Optional[torch.Tensor] = None, dW: Optional[torch.Tensor] = None,
+                   row_loss: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Draft LM head z = h W^T fused with the soft-CE: loss and the fp32 gradients
+    of h [N, Hd] and W [V, Hd] (both bf16), z never materialised.
+    Returns (loss [1], row_loss [N], dh [N, Hd], dW [V, Hd])."""
+    if h.dim() != 2 or W.dim() != 2:
+        raise ValueError("h must be [N, Hd] and W [V, Hd]")
+    N, Hd = h.shape
+    V = W.shape[0]
+    _need(h, "h", torch.bfloat16)
+    _need(W, "W", torch.bfloat16, (V, Hd))
+    _need(p, "p", torch.float32, (N, V))
+    _need(g, "g", torch.float32, (N,))
+    dev = h.device
+    if dh is None:
+        dh = torch.empty((N, Hd), device=dev, dtype=torch.float32)
+    if dW is None:
+        dW = torch.empty((V, Hd), device=dev, dtype=torch.float32)
+    if row_loss is None:
+        row_loss = torch.empty(N, device=dev, dtype=torch.float32)
+    if loss is None:
+        loss = torch.empty(1, device=dev, dtype=torch.float32)
+    _need(dh, "dh", torch.float32, (N, Hd))
+    _need(dW, "dW", torch.float32, (V, Hd))
+    _need(row_loss, "row_loss", torch.float32, (N,))
+    _need(loss, "loss", torch.float32)
+    need = int(lib().stt_lm_head_ce_workspace_size(N, Hd, V))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    st = lib().stt_lm_head_ce(_ptr(h), _ptr(W), _ptr(p), _ptr(g), N, Hd, V, _ptr(dh), _ptr(dW),
+                              _ptr(row_loss), _ptr(loss), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    check("stt_lm_head_ce", st)
+    return loss, row_loss, dh, dW
 
 
 def stt_verify(p_target: torch.Tensor, p_draft: torch.Tensor, draft_tokens: torch.Tensor,

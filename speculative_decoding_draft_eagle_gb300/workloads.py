@@ -200,3 +200,25 @@ def verify_inputs(vs: VerifyShape, device, seed: int):
     u_acc = torch.rand((vs.B, vs.gamma), generator=_gen(device, seed, 63), device=device)
     u_smp = torch.rand((vs.B,), generator=_gen(device, seed, 64), device=device)
     return p_t, p_d, toks, u_acc, u_smp
+
+
+@dataclasses.dataclass(frozen=True)
+class LmHeadShape:
+    """The draft's LM head and its soft-CE: N tokens, hidden size Hd, draft
+    vocabulary V.  h ~ N(0, 1) and W ~ N(0, 1/Hd) in bf16 (logits of unit
+    scale); the targets and g as the soft-CE workloads draw them."""
+    N: int
+    Hd: int
+    V: int
+
+
+# Llama-3.1-8B-shaped draft: hidden 4096, draft vocabulary 32000, 4096 tokens.
+LM_HEAD = LmHeadShape(N=4096, Hd=4096, V=32000)
+
+
+def lm_head_inputs(ls: LmHeadShape, device, seed: int):
+    """h bf16 [N, Hd], W bf16 [V, Hd], p fp32 [N, V], g fp32 [N]."""
+    h = randn_bf16((ls.N, ls.Hd), device, seed, 70)
+    W = randn_bf16((ls.V, ls.Hd), device, seed, 71, std=1.0 / math.sqrt(ls.Hd))
+    _, p, g = soft_ce_inputs(SoftCEShape(N=ls.N, V=ls.V), device, seed)
+    return h, W, p, g

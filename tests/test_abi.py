@@ -141,3 +141,15 @@ def test_verify_rejects_bad_arguments(L):
     assert f(good, good, good, good, good, 2, 5, 0, good, good, None) == -1
     assert f(None, good, good, good, good, 2, 5, 100, good, good, None) == -1
     assert f(good + 2, good, good, good, good, 2, 5, 100, good, good, None) == -3
+
+
+def test_lm_head_ce_rejects_bad_arguments(L):
+    good = 0x1000
+    f = L.stt_lm_head_ce
+    big = 1 << 30
+    assert f(good, good, good, good, -1, 64, 256, good, good, None, good, good, big, None) == -1
+    assert f(good, good, good, good, 8, 60, 256, good, good, None, good, good, big, None) == -2
+    assert f(good, good, good, good, 8, 64, 250, good, good, None, good, good, big, None) == -2
+    assert f(good, good, good, good, 8, 64, 256, good, good, None, good, None, 0, None) == -6
+    assert f(good + 8, good, good, good, 8, 64, 256, good, good, None, good, good, big, None) == -3
+    assert L.stt_lm_head_ce_workspace_size(4096, 4096, 32000) >= 4096 * 125 * 16
