@@ -22,9 +22,16 @@ Readings where the page is silent:
   * The test u < min(1, p_t / p_d) is evaluated as u * p_d < p_t in float64
     (exact for float32 inputs, and the same for p_d > 0); a draft token with
     p_d = 0 is accepted iff p_t > 0.
-  * Sampling from norm(r), r_v = max(0, p_t[v] - p_d[v]) (float64), with one
-    uniform u: the smallest y with r_0 + ... + r_y > u * sum(r) (inverse CDF).
-  * If sum(r) = 0 the draw is taken from p_t itself by the same rule
+  * Sampling from norm(r) with one uniform u is the inverse CDF, on weights
+    made exact so that the integer it decides does not depend on the order
+    of a sum: r_v = min(1, max(0, p_t[v] - p_d[v])) with the difference
+    rounded to float32, quantised to q_v = floor(r_v * 2^s) with
+    s = 62 - bitlen(V) (so sum(q) < 2^63; weights below 2^-s, at most
+    V * 2^-s of the mass, are dropped); u is quantised to
+    u24 = floor(u * 2^24); the threshold is t = floor(u24 * Q / 2^24) with
+    Q = sum(q), and the draw is the smallest y with q_0 + ... + q_y > t.
+    All of it is integer arithmetic.
+  * If Q = 0 the draw is taken from p_t itself by the same rule
     (convention: it arises only when p_t <= p_d everywhere).
   * A draft token outside [0, V) has probability 0 under both models, so it
     is never accepted (convention for invalid input).
@@ -34,25 +41,34 @@ Readings where the page is silent:
     n_acc < gamma, then -1.
 """
 
+import math
+
 import numpy as np
 
 
-def inverse_cdf(weights, u):
-    """Smallest index y with weights[0] + ... + weights[y] > u * sum(weights)
-    (plain sequential float64 sums); the last positive index if rounding puts
-    the threshold past the total."""
-    w = np.asarray(weights, dtype=np.float64)
-    total = float(w.sum())
-    thresh = float(u) * total
-    acc = 0.0
-    last = -1
-    for y in range(len(w)):
-        if w[y] > 0.0:
-            last = y
-        acc += float(w[y])
-        if acc > thresh:
+def quantised_weights(w, V):
+    """q_v = floor(min(1, max(0, w_v)) * 2^(62 - bitlen(V))) as Python ints;
+    w is float32 (the residual or the target row)."""
+    s = 62 - int(V).bit_length()
+    w = np.minimum(np.float32(1.0), np.maximum(np.float32(0.0), np.asarray(w, dtype=np.float32)))
+    return [int(math.floor(float(x) * 2.0 ** s)) for x in w]
+
+
+def inverse_cdf(q, u):
+    """Smallest index y with q[0] + ... + q[y] > floor(u24 * Q / 2^24), where
+    Q = sum(q) and u24 = floor(u * 2^24) (exact integer arithmetic); -1 if
+    Q = 0."""
+    Q = sum(q)
+    if Q == 0:
+        return -1
+    u24 = int(math.floor(float(np.float32(u)) * 2.0 ** 24))
+    t = (u24 * Q) >> 24
+    acc = 0
+    for y, x in enumerate(q):
+        acc += x
+        if acc > t:
             return y
-    return last
+    return -1
 
 
 def verify_row(p_t, p_d, tokens, u_accept, u_sample):
@@ -71,10 +87,12 @@ def verify_row(p_t, p_d, tokens, u_accept, u_sample):
         if accept:
             out[i] = x
             continue
-        r = np.maximum(0.0, p_t[i] - p_d[i])
-        if float(r.sum()) == 0.0:
-            r = p_t[i]
-        out[i] = inverse_cdf(r, u_sample)
+        # the residual, with the difference rounded to float32
+        r = np.asarray(p_t[i], dtype=np.float32) - np.asarray(p_d[i], dtype=np.float32)
+        q = quantised_weights(r, V)
+        if sum(q) == 0:
+            q = quantised_weights(np.asarray(p_t[i], dtype=np.float32), V)
+        out[i] = inverse_cdf(q, u_sample)
         return i, out
     return gamma, out
 

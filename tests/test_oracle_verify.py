@@ -41,9 +41,9 @@ def _first_token_distribution(p_t, p_d, M=400):
                 dist[out[0]] += p_d[x] / M
             else:
                 # the resampled token depends on u_sample only: integrate it
-                r = np.maximum(0.0, p_t - p_d)
+                q = ov.quantised_weights(np.float32(p_t) - np.float32(p_d), V)
                 for us_ in us:
-                    dist[ov.inverse_cdf(r, us_)] += p_d[x] / M / M
+                    dist[ov.inverse_cdf(q, us_)] += p_d[x] / M / M
     return dist
 
 
@@ -92,12 +92,29 @@ def test_resample_never_draws_where_draft_covers_target():
         assert n == 0 and p_t[out[0]] > p_d[out[0]]
 
 
-def test_inverse_cdf_is_searchsorted():
+def test_inverse_cdf_is_bisect():
+    """On the exact integer weights the draw is the standard library's
+    bisect_right of the threshold in the running sums."""
+    import bisect
+    import itertools
     rng = np.random.default_rng(6)
     for _ in range(100):
-        w = rng.uniform(0, 1, size=30) * (rng.uniform(size=30) < 0.6)
-        if w.sum() == 0:
+        w = (rng.uniform(0, 1, size=30) * (rng.uniform(size=30) < 0.6)).astype(np.float32)
+        q = ov.quantised_weights(w, 30)
+        if sum(q) == 0:
             continue
-        u = rng.uniform()
-        c = np.cumsum(w)
-        assert ov.inverse_cdf(w, u) == int(np.searchsorted(c, u * c[-1], side="right"))
+        u = np.float32(rng.uniform())
+        c = list(itertools.accumulate(q))
+        t = (int(np.floor(float(u) * 2 ** 24)) * c[-1]) >> 24
+        assert ov.inverse_cdf(q, u) == bisect.bisect_right(c, t)
+
+
+def test_quantised_weights_keep_the_distribution():
+    """The quantisation moves each weight by less than 2^-(62 - bitlen(V))."""
+    rng = np.random.default_rng(7)
+    V = 151936
+    w = rng.dirichlet(np.ones(V)).astype(np.float32)
+    q = ov.quantised_weights(w, V)
+    s = 62 - V.bit_length()
+    err = np.abs(np.array(q, dtype=np.float64) * 2.0 ** -s - w.astype(np.float64))
+    assert err.max() < 2.0 ** -s and sum(q) < 2 ** 63
