@@ -6,12 +6,17 @@
 //
 // One CTA per sequence.  Warp 0 makes all gamma tests at once (lane i loads
 // p_t[i, x_i] and p_d[i, x_i] and tests u_i p_d < p_t in fp64, exact for fp32
-// inputs); a ballot gives the first rejection.  Only then is a row read: the
-// CTA sums the residual r_v = max(0, p_t[v] - p_d[v]) in fp64 (one coalesced
-// pass over both rows), and walks the row again in tiles of 4 elements per
-// thread with a block-wide fp64 scan until the running sum passes
-// u_sample * sum(r): the inverse-CDF draw.  The second pass reads the rows
-// from L2 and stops at the drawn token.
+// inputs); a ballot gives the first rejection.  Only then is a row read.  The
+// draw is an inverse CDF over exact integer weights, so the token it decides
+// does not depend on the order of any floating-point sum: the residual
+// r_v = min(1, max(0, p_t[v] - p_d[v])) (difference rounded to fp32) becomes
+// q_v = floor(r_v 2^s), s = 62 - bitlen(V), so every running sum is an exact
+// int64 below 2^63.  The CTA sums q in one coalesced pass over both rows, forms
+// the threshold t = floor(u24 Q / 2^24) (u24 = floor(u 2^24), a 128-bit
+// product), and walks the row again in tiles of 4 elements per thread with a
+// block-wide int64 scan until the running sum passes t.  The second pass
+// reads the rows from L2 and stops at the drawn token.  (fp64 is avoided on
+// the row: its rate on this GPU is a small fraction of fp32's.)
 #include <cstdint>
 
 #include "../../include/stt.h"
@@ -33,37 +38,39 @@ struct VerifyParams {
   int32_t* out;            // [B, gamma]
   long long V;
   int gamma;
+  int shift;  // s = 62 - bitlen(V): weights are floor(w 2^s)
 };
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Residual weight of element v (fp64, exact for fp32 inputs); with `target`
-// the weights are p_t itself (the draw when the residual sums to zero).
-__device__ __forceinline__ double weight(float pt, float pd, bool target) {
-  const double d = target ? (double)pt : (double)pt - (double)pd;
-  return d > 0.0 ? d : 0.0;
+// Quantised weight of element v: floor(min(1, max(0, w)) 2^s) with w the
+// fp32 residual p_t - p_d (or p_t itself when `target`).
+__device__ __forceinline__ long long qweight(float pt, float pd, bool target, float scale) {
+  float w = target ? pt : __fsub_rn(pt, pd);
+  w = fminf(1.0f, fmaxf(0.0f, w));
+  return __float2ll_rz(__fmul_rn(w, scale));  // exact: scale is a power of two
 }
 
-// Inclusive block-wide scan of one fp64 value per thread; returns the
-// exclusive prefix and stores the block total in *total (all threads).
-__device__ __forceinline__ double block_scan_excl(double v, double* s_warp, double* total) {
+// Exclusive block-wide scan of one int64 per thread; *total receives the sum.
+__device__ __forceinline__ long long block_scan_excl(long long v, long long* s_warp,
+                                                     long long* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = v;
+  long long incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xffffffffu, incl, o);
+    const long long t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  double before = 0.0, all = 0.0;
+  long long before = 0, all = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    const double x = s_warp[w];
+    const long long x = s_warp[w];
     if (w < warp) before += x;
     all += x;
   }
@@ -75,9 +82,8 @@ __device__ __forceinline__ double block_scan_excl(double v, double* s_warp, doub
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) {
   __shared__ int s_rej;
-  __shared__ double s_warp[kWarps];
-  __shared__ double s_red[kWarps];
-  __shared__ int s_last;
+  __shared__ long long s_warp[kWarps];
+  __shared__ long long s_red[kWarps];
   __shared__ int s_found;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -103,7 +109,6 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
     const unsigned m = __ballot_sync(0xffffffffu, reject);
     if (lane == 0) {
       s_rej = m ? __ffs((int)m) - 1 : gamma;
-      s_last = -1;
       s_found = 0;
     }
   }
@@ -116,85 +121,77 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   // ---- the draw at position r
   const float* pt_row = P.p_t + (b * gamma + r) * V;
   const float* pd_row = P.p_d + (b * gamma + r) * V;
+  const float scale = __uint_as_float((uint32_t)(127 + P.shift) << 23);  // 2^s
   bool target = false;
-  double R = 0.0;
+  long long Q = 0;
   for (int pass = 0; pass < 2; ++pass) {
-    // sum of the weights, and the last index with a positive weight
-    double s = 0.0;
-    int last = -1;
+    long long s = 0;
     if constexpr (VEC) {
       const float4* t4 = reinterpret_cast<const float4*>(pt_row);
       const float4* d4 = reinterpret_cast<const float4*>(pd_row);
       for (long long i = tid; i < V / 4; i += kThreads) {
         const float4 a = __ldg(t4 + i), c = __ldg(d4 + i);
-        const double w0 = weight(a.x, c.x, target), w1 = weight(a.y, c.y, target);
-        const double w2 = weight(a.z, c.z, target), w3 = weight(a.w, c.w, target);
-        s += (w0 + w1) + (w2 + w3);
-        if (w3 > 0.0) last = (int)(4 * i + 3);
-        else if (w2 > 0.0) last = (int)(4 * i + 2);
-        else if (w1 > 0.0) last = (int)(4 * i + 1);
-        else if (w0 > 0.0) last = (int)(4 * i);
+        s += qweight(a.x, c.x, target, scale) + qweight(a.y, c.y, target, scale) +
+             qweight(a.z, c.z, target, scale) + qweight(a.w, c.w, target, scale);
       }
     } else {
-      for (long long i = tid; i < V; i += kThreads) {
-        const double w = weight(__ldg(pt_row + i), __ldg(pd_row + i), target);
-        s += w;
-        if (w > 0.0) last = (int)i;
-      }
+      for (long long i = tid; i < V; i += kThreads)
+        s += qweight(__ldg(pt_row + i), __ldg(pd_row + i), target, scale);
     }
-    s = warp_sum_d(s);
+    s = warp_sum_ll(s);
     if (lane == 0) s_red[warp] = s;
-    if (last >= 0) atomicMax(&s_last, last);
     __syncthreads();
-    R = 0.0;
+    Q = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) R += s_red[w];
+    for (int w = 0; w < kWarps; ++w) Q += s_red[w];
     __syncthreads();
-    if (R > 0.0 || target) break;
+    if (Q > 0 || target) break;
     target = true;  // the residual is empty: draw from p_t itself
-    if (tid == 0) s_last = -1;
-    __syncthreads();
   }
-  const double thresh = (double)P.u_sample[b] * R;
+  if (Q == 0) {  // nothing to draw from (an all-zero target row)
+    if (tid == 0) P.out[b * gamma + r] = -1;
+    return;
+  }
+  // t = floor(u24 Q / 2^24) with u24 = floor(u 2^24), from the 128-bit product
+  const unsigned long long u24 =
+      (unsigned long long)__float2ll_rz(__fmul_rn(P.u_sample[b], 16777216.0f));
+  const unsigned long long lo = u24 * (unsigned long long)Q;
+  const unsigned long long hi = __umul64hi(u24, (unsigned long long)Q);
+  const long long thresh = (long long)((hi << 40) | (lo >> 24));
 
   // Second walk: tiles of kThreads * E elements, block-wide scan per tile.
   constexpr int E = VEC ? 4 : 1;
-  double running = 0.0;
+  long long running = 0;
   for (long long base = 0; base < V; base += (long long)kThreads * E) {
     const long long i0 = base + (long long)tid * E;
-    double w[E];
+    long long w[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) w[e] = 0.0;
+    for (int e = 0; e < E; ++e) w[e] = 0;
     if (i0 < V) {
       if constexpr (VEC) {
         const float4 a = __ldg(reinterpret_cast<const float4*>(pt_row + i0));
         const float4 c = __ldg(reinterpret_cast<const float4*>(pd_row + i0));
-        w[0] = weight(a.x, c.x, target);
-        w[1] = weight(a.y, c.y, target);
-        w[2] = weight(a.z, c.z, target);
-        w[3] = weight(a.w, c.w, target);
+        w[0] = qweight(a.x, c.x, target, scale);
+        w[1] = qweight(a.y, c.y, target, scale);
+        w[2] = qweight(a.z, c.z, target, scale);
+        w[3] = qweight(a.w, c.w, target, scale);
       } else {
-        w[0] = weight(__ldg(pt_row + i0), __ldg(pd_row + i0), target);
+        w[0] = qweight(__ldg(pt_row + i0), __ldg(pd_row + i0), target, scale);
       }
     }
-    double mine = 0.0;
+    long long mine = 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) mine += w[e];
-    double tile_total;
-    const double before = running + block_scan_excl(mine, s_warp, &tile_total);
-    // the crossing lies in this thread's elements: before <= thresh < before + mine
-    if (mine > 0.0 && before <= thresh && thresh < before + mine) {
-      double acc = before;
+    long long tile_total;
+    const long long before = running + block_scan_excl(mine, s_warp, &tile_total);
+    // the crossing lies in this thread's elements: before <= t < before + mine
+    if (before <= thresh && thresh < before + mine) {
+      long long acc = before;
       int y = -1;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         acc += w[e];
         if (y < 0 && acc > thresh) y = (int)(i0 + e);
-      }
-      if (y < 0) {  // rounding inside the thread's partial sum: its last positive element
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (w[e] > 0.0) y = (int)(i0 + e);
       }
       P.out[b * gamma + r] = y;
       s_found = 1;
@@ -203,9 +200,6 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
     __syncthreads();
     if (s_found) return;
   }
-  // The threshold fell past the (block-order) total by rounding: the last
-  // positive weight.
-  if (tid == 0) P.out[b * gamma + r] = s_last;
 }
 
 }  // namespace
@@ -213,7 +207,9 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
 cudaError_t verify_launch(const float* p_t, const float* p_d, const int32_t* tokens,
                           const float* u_accept, const float* u_sample, int B, int gamma,
                           int64_t V, int32_t* n_acc, int32_t* out, cudaStream_t s) {
-  VerifyParams P{p_t, p_d, tokens, u_accept, u_sample, n_acc, out, (long long)V, gamma};
+  int bits = 0;
+  for (long long v = V; v > 0; v >>= 1) ++bits;
+  VerifyParams P{p_t, p_d, tokens, u_accept, u_sample, n_acc, out, (long long)V, gamma, 62 - bits};
   const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(p_t) & 15u) == 0) &&
                    ((reinterpret_cast<uintptr_t>(p_d) & 15u) == 0);
   prof_before(s, STT_KERNEL_VERIFY);
