@@ -64,6 +64,10 @@ def parse():
     ap.add_argument("--no-other-workloads", action="store_true")
     ap.add_argument("--other-steps", type=int, default=5)
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--profile", choices=["attn", "lm_head", "verify"], default=None,
+                    help="small profiling case (a few GB): 2 calls of one row and exit")
+    ap.add_argument("--profile-step", type=int, default=None,
+                    help="with --profile attn: the TTT step (default: the workload's last)")
     a = ap.parse_args()
     if a.warmup < 0 or a.steps < 1:
         ap.error("--steps must be >= 1 and --warmup >= 0")
@@ -741,9 +745,43 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(a):
+    """Two calls of one row on bounded memory, for ncu captures: the attention
+    forward + backward at one TTT step of the workload (inputs of that step
+    only), the fused LM head, or the verifier.  Prints nothing measured."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    from speculative_decoding_draft_eagle_gb300 import build, ops
+    build.build()
+    if a.profile == "attn":
+        w = wl.WORKLOADS[a.workload]
+        sh = w.attn
+        k = sh.steps[-1] if a.profile_step is None else a.profile_step
+        T = wl.draw_T(sh, w.seed)
+        Ks = [wl.kv_block(sh, "K", j, dev, w.seed) for j in range(k + 1)]
+        Vs = [wl.kv_block(sh, "V", j, dev, w.seed) for j in range(k + 1)]
+        q, dO = wl.step_query(sh, k, dev, w.seed), wl.step_dout(sh, k, dev, w.seed)
+        for _ in range(2):
+            out, lse = ops.stt_attn_fwd(q, Ks, Vs, T, sh.scale)
+            ops.stt_attn_bwd(q, Ks, Vs, T, out, dO, lse, sh.scale)
+    elif a.profile == "lm_head":
+        h, W, p, g = wl.lm_head_inputs(wl.LM_HEAD, dev, 1002)
+        for _ in range(2):
+            ops.stt_lm_head_ce(h, W, p, g)
+    else:
+        args = wl.verify_inputs(wl.VERIFY, dev, 1006)
+        for _ in range(2):
+            ops.stt_verify(*args)
+    torch.cuda.synchronize()
+    assert ops.stt_device_error() == 0
+    print(f"profile case {a.profile} done", flush=True)
+
+
 def main():
     a = parse()
-    if a.impl == "reference":
+    if a.profile:
+        run_profile_case(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)
