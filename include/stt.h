@@ -342,8 +342,10 @@ STT_API int stt_lm_head_ce(const void* h, const void* W, const float* p, const f
  *  out_tokens int32 [B, gamma]: the accepted tokens, then the drawn token if
  *             n_accepted < gamma, then -1.
  * All pointers device, 4-byte aligned (rows that are 16-byte aligned with
- * V % 4 == 0 are read with 16-byte loads).  The random numbers are inputs,
- * so a call is deterministic.
+ * V % 4 == 0 are read with 16-byte loads).  V above 16 x 51200 returns
+ * STT_ERR_UNSUPPORTED (a rejected row is split over at most 16 CTAs, each
+ * holding its slice in shared memory).  The random numbers are inputs, so a
+ * call is deterministic.
  * ------------------------------------------------------------------------ */
 #define STT_VERIFY_MAX_GAMMA 32
 STT_API int stt_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,

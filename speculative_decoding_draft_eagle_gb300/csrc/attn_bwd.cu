@@ -39,7 +39,10 @@ constexpr int kThreads = 480;
 constexpr int kCompute = 256;
 constexpr int kComputeWarps = kCompute / 32;  // barriers count one arrival per warp
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpEpi = 10, kWarpMma2 = 14;
-constexpr int kHeadChunk = 16;  // heads per group of key-tile CTAs scheduled together
+// Heads per group of key-tile CTAs scheduled together: as many as keep their
+// Q, dO (bf16) and dq (fp32) -- 8 bytes per element -- within kChunkBytes of L2.
+constexpr long long kChunkBytes = 64ll << 20;
+constexpr int kHeadChunkMax = 16;
 constexpr int kEpiWarps = 4;  // one per TMEM lane quarter (warp % 4)
 
 struct BwdParams {
@@ -56,6 +59,7 @@ struct BwdParams {
   float* dv0;
   float* delta;
   int B, H, H_kv, Q_LEN, k, n_t, G;
+  int head_chunk;           // heads per group of key-tile CTAs scheduled together
   int accumulate;           // add into dK_j / dV_j, j >= 1 (read-modify-write)
   int zero_acc0;            // the prep kernel zeroes dk0 / dv0 first
   float scale, scale_log2;
@@ -433,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float s_stat[2][2][kTile];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Heads are taken in chunks of kHeadChunk: the CTAs of one chunk run
-  // together and re-read only their heads' Q and dO (16 heads x 2 x Q_LEN x D
-  // bf16 stay in L2), and within a chunk the key tiles go longest first.
+  // Heads are taken in chunks of P.head_chunk: the CTAs of one chunk run
+  // together and re-read only their heads' Q and dO, and add into only their
+  // heads' dq, which stay in L2; within a chunk the key tiles go longest first.
   const int nb = P.H * P.B;
-  const int ch = nb < kHeadChunk ? nb : kHeadChunk;
+  const int ch = nb < P.head_chunk ? nb : P.head_chunk;
   const int chunk = (int)(blockIdx.x / (unsigned)(P.n_t * ch));
   const int chunk_heads = min(ch, nb - chunk * ch);
   const int rem = (int)blockIdx.x - chunk * P.n_t * ch;
@@ -965,6 +969,11 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   P.k = a.k;
   P.n_t = (a.Q_LEN + kTile - 1) / kTile;
   P.G = a.H / a.H_kv;
+  {
+    const long long per_head = (long long)a.Q_LEN * D * 8;
+    long long ch = kChunkBytes / (per_head > 0 ? per_head : 1);
+    P.head_chunk = (int)(ch < 1 ? 1 : (ch > kHeadChunkMax ? kHeadChunkMax : ch));
+  }
   P.scale = a.scale;
   P.scale_log2 = a.scale * kLog2e;
   for (int b = 0; b < a.B; ++b) P.T[b] = a.T[b];

@@ -4,29 +4,38 @@
 // min(1, p_t[x_i] / p_d[x_i]); at the first rejection one token is drawn from
 // norm(max(0, p_t - p_d)) at that position and the sequence stops.
 //
-// One CTA per sequence.  Warp 0 makes all gamma tests at once (lane i loads
+// One thread-block cluster of C CTAs per sequence; CTA c owns a slice of the
+// vocabulary.  Warp 0 of every CTA makes all gamma tests at once (lane i loads
 // p_t[i, x_i] and p_d[i, x_i] and tests u_i p_d < p_t in fp64, exact for fp32
-// inputs); a ballot gives the first rejection.  Only then is a row read.  The
-// draw is an inverse CDF over exact integer weights, so the token it decides
-// does not depend on the order of any floating-point sum: the residual
+// inputs); a ballot gives the first rejection, the same in every CTA, so a
+// sequence whose tokens are all accepted reads nothing more.  At a rejection
+// the draw is an inverse CDF over exact integer weights, so the token it
+// decides does not depend on the order of any sum: the residual
 // r_v = min(1, max(0, p_t[v] - p_d[v])) (difference rounded to fp32) becomes
-// q_v = floor(r_v 2^s), s = 62 - bitlen(V), so every running sum is an exact
-// int64 below 2^63.  The CTA sums q in one coalesced pass over both rows, forms
-// the threshold t = floor(u24 Q / 2^24) (u24 = floor(u 2^24), a 128-bit
-// product), and walks the row again in tiles of 4 elements per thread with a
-// block-wide int64 scan until the running sum passes t.  The second pass
-// reads the rows from L2 and stops at the drawn token.  (fp64 is avoided on
-// the row: its rate on this GPU is a small fraction of fp32's.)
+// q_v = floor(r_v 2^s), s = 62 - bitlen(V), and every running sum is an exact
+// int64 below 2^63.  Each CTA streams its slice of both rows once (coalesced
+// 16-byte loads), keeps the fp32 residuals in shared memory and sums its q;
+// the C slice sums are exchanged through distributed shared memory, giving the
+// total Q and each slice's prefix; the threshold is t = floor(u24 Q / 2^24)
+// (u24 = floor(u 2^24), a 128-bit product); only the CTA whose prefix range
+// holds t scans its slice (from shared memory: one block-wide scan of the
+// threads' contiguous runs, then the thread whose run holds t walks it) for
+// the smallest y whose running sum exceeds t.  fp64 is kept off the rows:
+// its rate on this GPU is a small fraction of fp32's.
 #include <cstdint>
 
 #include "../../include/stt.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace stt {
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 16;
+constexpr int kSliceTarget = 16384;   // preferred elements per CTA (64 KB of residuals)
+constexpr int kSliceMax = 50 * 1024;  // elements per CTA at most (200 KB)
 
 struct VerifyParams {
   const float* p_t;        // [B, gamma, V]
@@ -38,7 +47,9 @@ struct VerifyParams {
   int32_t* out;            // [B, gamma]
   long long V;
   int gamma;
-  int shift;  // s = 62 - bitlen(V): weights are floor(w 2^s)
+  int shift;               // s = 62 - bitlen(V): weights are floor(w 2^s)
+  int C;                   // CTAs per sequence (cluster size)
+  int slice;               // elements per CTA (a multiple of 4)
 };
 
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
@@ -47,12 +58,26 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
   return v;
 }
 
-// Quantised weight of element v: floor(min(1, max(0, w)) 2^s) with w the
-// fp32 residual p_t - p_d (or p_t itself when `target`).
-__device__ __forceinline__ long long qweight(float pt, float pd, bool target, float scale) {
-  float w = target ? pt : __fsub_rn(pt, pd);
-  w = fminf(1.0f, fmaxf(0.0f, w));
+// The fp32 weight of an element: the residual p_t - p_d rounded to fp32, or
+// p_t itself when `target`, clamped to [0, 1].
+__device__ __forceinline__ float fweight(float pt, float pd, bool target) {
+  const float w = target ? pt : __fsub_rn(pt, pd);
+  return fminf(1.0f, fmaxf(0.0f, w));
+}
+__device__ __forceinline__ long long quant(float w, float scale) {
   return __float2ll_rz(__fmul_rn(w, scale));  // exact: scale is a power of two
+}
+
+// Block-wide sum of one int64 per thread (every thread gets it).
+__device__ __forceinline__ long long block_sum(long long v, long long* s_warp) {
+  v = warp_sum_ll(v);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = v;
+  __syncthreads();
+  long long all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) all += s_warp[w];
+  __syncthreads();
+  return all;
 }
 
 // Exclusive block-wide scan of one int64 per thread; *total receives the sum.
@@ -74,24 +99,72 @@ __device__ __forceinline__ long long block_scan_excl(long long v, long long* s_w
     if (w < warp) before += x;
     all += x;
   }
-  __syncthreads();  // s_warp is reused by the next call
+  __syncthreads();
   *total = all;
   return before + incl - v;
 }
 
+// Sum of the quantised weights of this CTA's slice [0, len), read from global
+// memory; the fp32 weights are kept in shared memory for the scan.
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) {
+__device__ __forceinline__ long long slice_weights(const float* pt, const float* pd, int len,
+                                                   bool target, float scale, float* sw,
+                                                   long long* s_warp) {
+  long long s = 0;
+  if constexpr (VEC) {
+    const float4* t4 = reinterpret_cast<const float4*>(pt);
+    const float4* d4 = reinterpret_cast<const float4*>(pd);
+    float4* w4 = reinterpret_cast<float4*>(sw);
+    const int n4 = len / 4;
+    // kBatch float4 of each row in flight per thread (half a slice of
+    // kSliceTarget elements per batch; registers for two CTAs per SM)
+    constexpr int kBatch = kSliceTarget / 8 / kThreads;
+    for (int base = 0; base < n4; base += kBatch * kThreads) {
+      float4 a[kBatch], c[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kThreads + threadIdx.x;
+        if (i < n4) {
+          a[u] = __ldg(t4 + i);
+          c[u] = __ldg(d4 + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kThreads + threadIdx.x;
+        if (i < n4) {
+          const float4 w = make_float4(fweight(a[u].x, c[u].x, target), fweight(a[u].y, c[u].y, target),
+                                       fweight(a[u].z, c[u].z, target), fweight(a[u].w, c[u].w, target));
+          w4[i] = w;
+          s += quant(w.x, scale) + quant(w.y, scale) + quant(w.z, scale) + quant(w.w, scale);
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < len; i += kThreads) {
+      const float w = fweight(__ldg(pt + i), __ldg(pd + i), target);
+      sw[i] = w;
+      s += quant(w, scale);
+    }
+  }
+  return block_sum(s, s_warp);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const VerifyParams P) {
+  extern __shared__ __align__(16) float sw[];  // this CTA's fp32 weights
   __shared__ int s_rej;
   __shared__ long long s_warp[kWarps];
-  __shared__ long long s_red[kWarps];
-  __shared__ int s_found;
+  __shared__ __align__(16) long long s_sum;   // read by the other CTAs of the cluster
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long b = blockIdx.x;
+  const int C = P.C;
+  const int rank = C > 1 ? (int)cluster_ctarank() : 0;
+  const long long b = blockIdx.x / C;
   const int gamma = P.gamma;
   const long long V = P.V;
 
-  // ---- the gamma acceptance tests, one lane each
+  // ---- the gamma acceptance tests, one lane each (the same in every CTA)
   if (warp == 0) {
     bool reject = false;
     if (lane < gamma) {
@@ -107,49 +180,51 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
       reject = !accept;
     }
     const unsigned m = __ballot_sync(0xffffffffu, reject);
-    if (lane == 0) {
-      s_rej = m ? __ffs((int)m) - 1 : gamma;
-      s_found = 0;
-    }
+    if (lane == 0) s_rej = m ? __ffs((int)m) - 1 : gamma;
   }
   __syncthreads();
   const int r = s_rej;
-  if (tid < gamma) P.out[b * gamma + tid] = tid < r ? P.tokens[b * gamma + tid] : -1;
-  if (tid == 0) P.n_acc[b] = r;
-  if (r == gamma) return;
+  if (rank == 0) {
+    if (tid < gamma) P.out[b * gamma + tid] = tid < r ? P.tokens[b * gamma + tid] : -1;
+    if (tid == 0) P.n_acc[b] = r;
+  }
+  if (r == gamma) return;  // the same in every CTA of the cluster: no exchange follows
 
   // ---- the draw at position r
-  const float* pt_row = P.p_t + (b * gamma + r) * V;
-  const float* pd_row = P.p_d + (b * gamma + r) * V;
+  const long long begin = (long long)rank * P.slice;
+  const long long rem = V - begin;
+  const int len = rem <= 0 ? 0 : (rem < P.slice ? (int)rem : P.slice);
+  const float* pt_row = P.p_t + (b * gamma + r) * V + begin;
+  const float* pd_row = P.p_d + (b * gamma + r) * V + begin;
   const float scale = __uint_as_float((uint32_t)(127 + P.shift) << 23);  // 2^s
   bool target = false;
-  long long Q = 0;
+  long long Q = 0, prefix = 0, mine = 0;
   for (int pass = 0; pass < 2; ++pass) {
-    long long s = 0;
-    if constexpr (VEC) {
-      const float4* t4 = reinterpret_cast<const float4*>(pt_row);
-      const float4* d4 = reinterpret_cast<const float4*>(pd_row);
-      for (long long i = tid; i < V / 4; i += kThreads) {
-        const float4 a = __ldg(t4 + i), c = __ldg(d4 + i);
-        s += qweight(a.x, c.x, target, scale) + qweight(a.y, c.y, target, scale) +
-             qweight(a.z, c.z, target, scale) + qweight(a.w, c.w, target, scale);
+    mine = slice_weights<VEC>(pt_row, pd_row, len, target, scale, sw, s_warp);
+    Q = mine;
+    prefix = 0;
+    if (C > 1) {
+      if (tid == 0) s_sum = mine;
+      cluster_arrive_release();
+      cluster_wait_acquire();
+      Q = 0;
+      for (int c = 0; c < C; ++c) {
+        const uint32_t a = mapa_shared(smem_u32(&s_sum), (uint32_t)c);
+        long long v;
+        asm volatile("ld.shared::cluster.b64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+        if (c < rank) prefix += v;
+        Q += v;
       }
-    } else {
-      for (long long i = tid; i < V; i += kThreads)
-        s += qweight(__ldg(pt_row + i), __ldg(pd_row + i), target, scale);
+      // every CTA has read every slice sum before s_sum is written again or a
+      // CTA exits
+      cluster_arrive_release();
+      cluster_wait_acquire();
     }
-    s = warp_sum_ll(s);
-    if (lane == 0) s_red[warp] = s;
-    __syncthreads();
-    Q = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) Q += s_red[w];
-    __syncthreads();
     if (Q > 0 || target) break;
     target = true;  // the residual is empty: draw from p_t itself
   }
   if (Q == 0) {  // nothing to draw from (an all-zero target row)
-    if (tid == 0) P.out[b * gamma + r] = -1;
+    if (rank == 0 && tid == 0) P.out[b * gamma + r] = -1;
     return;
   }
   // t = floor(u24 Q / 2^24) with u24 = floor(u 2^24), from the 128-bit product
@@ -158,47 +233,27 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   const unsigned long long lo = u24 * (unsigned long long)Q;
   const unsigned long long hi = __umul64hi(u24, (unsigned long long)Q);
   const long long thresh = (long long)((hi << 40) | (lo >> 24));
+  if (!(prefix <= thresh && thresh < prefix + mine)) return;  // not in this slice
 
-  // Second walk: tiles of kThreads * E elements, block-wide scan per tile.
-  constexpr int E = VEC ? 4 : 1;
-  long long running = 0;
-  for (long long base = 0; base < V; base += (long long)kThreads * E) {
-    const long long i0 = base + (long long)tid * E;
-    long long w[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) w[e] = 0;
-    if (i0 < V) {
-      if constexpr (VEC) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(pt_row + i0));
-        const float4 c = __ldg(reinterpret_cast<const float4*>(pd_row + i0));
-        w[0] = qweight(a.x, c.x, target, scale);
-        w[1] = qweight(a.y, c.y, target, scale);
-        w[2] = qweight(a.z, c.z, target, scale);
-        w[3] = qweight(a.w, c.w, target, scale);
-      } else {
-        w[0] = qweight(__ldg(pt_row + i0), __ldg(pd_row + i0), target, scale);
+  // This CTA holds the crossing: every thread sums a contiguous run of the
+  // slice, one block-wide scan places the runs, and the thread whose run holds
+  // the threshold walks it.
+  __syncthreads();  // the weights in shared memory are complete
+  const int per = (len + kThreads - 1) / kThreads;
+  const int i0 = tid * per, i1 = min(len, i0 + per);
+  long long run = 0;
+  for (int i = i0; i < i1; ++i) run += quant(sw[i], scale);
+  long long total;
+  const long long before = prefix + block_scan_excl(run, s_warp, &total);
+  if (before <= thresh && thresh < before + run) {
+    long long acc = before;
+    for (int i = i0; i < i1; ++i) {
+      acc += quant(sw[i], scale);
+      if (acc > thresh) {
+        P.out[b * gamma + r] = (int)(begin + i);
+        break;
       }
     }
-    long long mine = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) mine += w[e];
-    long long tile_total;
-    const long long before = running + block_scan_excl(mine, s_warp, &tile_total);
-    // the crossing lies in this thread's elements: before <= t < before + mine
-    if (before <= thresh && thresh < before + mine) {
-      long long acc = before;
-      int y = -1;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        acc += w[e];
-        if (y < 0 && acc > thresh) y = (int)(i0 + e);
-      }
-      P.out[b * gamma + r] = y;
-      s_found = 1;
-    }
-    running += tile_total;
-    __syncthreads();
-    if (s_found) return;
   }
 }
 
@@ -209,15 +264,44 @@ cudaError_t verify_launch(const float* p_t, const float* p_d, const int32_t* tok
                           int64_t V, int32_t* n_acc, int32_t* out, cudaStream_t s) {
   int bits = 0;
   for (long long v = V; v > 0; v >>= 1) ++bits;
-  VerifyParams P{p_t, p_d, tokens, u_accept, u_sample, n_acc, out, (long long)V, gamma, 62 - bits};
+  long long C = (V + kSliceTarget - 1) / kSliceTarget;
+  if (C < 1) C = 1;
+  if (C > kMaxCluster) C = kMaxCluster;
+  long long slice = ((V + C - 1) / C + 3) / 4 * 4;
+  while (C > 1 && (C - 1) * slice >= V) {
+    --C;
+    slice = ((V + C - 1) / C + 3) / 4 * 4;
+  }
+  if (slice > kSliceMax) return cudaErrorNotSupported;
+  if ((long long)B * C > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(p_t) & 15u) == 0) &&
                    ((reinterpret_cast<uintptr_t>(p_d) & 15u) == 0);
+  VerifyParams P{p_t, p_d, tokens, u_accept, u_sample, n_acc, out, (long long)V, gamma, 62 - bits,
+                 (int)C, (int)slice};
+  void (*kern)(const VerifyParams) = vec ? verify_kernel<true> : verify_kernel<false>;
+  const int smem = (int)(slice * 4);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before(s, STT_KERNEL_VERIFY);
-  if (vec)
-    verify_kernel<true><<<(unsigned)B, kThreads, 0, s>>>(P);
-  else
-    verify_kernel<false><<<(unsigned)B, kThreads, 0, s>>>(P);
+  e = cudaLaunchKernelEx(&cfg, kern, P);
   prof_after(s);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
