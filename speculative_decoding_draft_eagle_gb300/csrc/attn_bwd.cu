@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stg_full.  MMA -> MMA: pt_free.  Issuers: drain.  Compute group: grp.
   __shared__ uint64_t bar_kv, bar_q_full[NS], bar_do_full[NS], bar_s_full,
       bar_dp_full, bar_p_ready, bar_pt_free, bar_ds_ready, bar_dq_full, bar_dk_done, bar_dq_free,
-      bar_stg_full, bar_stg_done, bar_final, bar_drain, bar_grp;
+      bar_stg_full[2], bar_stg_done, bar_final, bar_drain, bar_grp;
   __shared__ uint32_t tmem_base;
   // [tile parity][-lse2 | -Delta][query]: tile i's statistics sit in buffer i & 1.
   __shared__ __align__(16) float s_stat[2][2][kTile];
@@ -467,7 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dk_done, 1);
     mbar_init(&bar_dq_free, kEpiWarps);
-    mbar_init(&bar_stg_full, kEpiWarps);
+    // stg_full alternates by tile parity: the epilogue warps meet no other
+    // barrier between one tile's staging and the next, so one of them could
+    // arrive for tile i + 1 before another has arrived for tile i.
+    mbar_init(&bar_stg_full[0], kEpiWarps);
+    mbar_init(&bar_stg_full[1], kEpiWarps);
     mbar_init(&bar_final, 1);
     mbar_init(&bar_stg_done, 1);  // producer: every dQ staging read by TMA
     mbar_init(&bar_drain, 2);  // one commit from each issuing thread
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tq0 = (t_first + i) * kTile;
         const bool more = i + NS < n_q;
         // dQ of tile i, staged in its Q and dO buffers (dK(i) and dV(i) done).
-        ok = mbar_wait(&bar_stg_full, (uint32_t)i & 1u, STT_DEVERR_BWD_WAIT);
+        ok = mbar_wait(&bar_stg_full[i & 1], (uint32_t)(i >> 1) & 1u, STT_DEVERR_BWD_WAIT);
         if (!ok) break;
         // Part A first; Q(i + NS) follows as soon as TMA has read it, ahead of
         // part B in TMA's queue, since S^T(i + NS) needs it first.
@@ -700,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage(dq_staging<D>(smem, 0, 0, st), a0);
       stage(dq_staging<D>(smem, 0, 1, st), a1);
       fence_proxy_async_smem();
-      warp_arrive(&bar_stg_full);
+      warp_arrive(&bar_stg_full[i & 1]);
     }
   } else {
     // ------------------------------------------------------ compute warps --

@@ -100,6 +100,10 @@ cudaError_t soft_ce_set_wait_budget(uint64_t ns);
 cudaError_t attn_fwd_set_wait_budget(uint64_t ns);
 cudaError_t attn_bwd_set_wait_budget(uint64_t ns);
 
+// Streaming multiprocessors of the current device (cached per device; 1 if
+// the query fails, which only shrinks persistent grids).
+int sm_count();
+
 // Test hooks set by stt_debug_inject (STT_INJECT_* bits), read at launch.
 uint32_t debug_inject();
 

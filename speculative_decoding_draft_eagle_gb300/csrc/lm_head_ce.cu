@@ -369,19 +369,6 @@ __global__ void __launch_bounds__(256) lm_combine_kernel(const float4* part, int
   }
 }
 
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      return 148;
-  }
-  return n;
-}
-
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t run_gemm(GemmP P, const CUtensorMap& tmA, const CUtensorMap& tmB, cudaStream_t s) {
   P.tiles_m = (P.M + BM - 1) / BM;
@@ -392,7 +379,7 @@ cudaError_t run_gemm(GemmP P, const CUtensorMap& tmA, const CUtensorMap& tmB, cu
   auto kern = lm_gemm_kernel<A_MN, B_MN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int grid = tiles < sm_count() ? tiles : sm_count();
   kern<<<grid, kGThreads, kSmem, s>>>(P, tmA, tmB);
   return cudaGetLastError();
 }

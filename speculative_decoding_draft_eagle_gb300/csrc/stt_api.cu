@@ -35,7 +35,22 @@ cudaError_t bind_device_context() {
 
 namespace {
 std::atomic<uint32_t> g_inject{0};
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
 }  // namespace
+
+int sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 1;
+  if (dev < kMaxDevices) g_sm_count[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
 
 uint32_t debug_inject() { return g_inject.load(std::memory_order_relaxed); }
 

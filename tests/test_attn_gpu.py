@@ -120,6 +120,29 @@ def check_bwd(q, Ks, Vs, dO, T, scale):
         close(f64(dv[j]), rv[j], f"dV[{j}]", atol=bound(ev[j], rv[j]), group="attention shapes (bwd)")
 
 
+@pytest.mark.parametrize("name", ["varlen", "llama8b"])
+def test_forward_repeats_bit_identical(name):
+    """The forward has no atomics and a fixed work order, so repeated launches
+    on the same inputs must give bit-identical O and lse.  The persistent
+    kernel carries every barrier phase across work items; a waiter that reads
+    a phase too early (the many short items of varlen make item boundaries
+    frequent) shows up here as rows that differ between launches."""
+    w = wl.WORKLOADS[name]
+    sh = w.attn
+    T = wl.draw_T(sh, w.seed)
+    Ks = [wl.kv_block(sh, "K", j, DEV, w.seed) for j in range(sh.n_blocks)]
+    Vs = [wl.kv_block(sh, "V", j, DEV, w.seed) for j in range(sh.n_blocks)]
+    for k in (0, max(sh.steps)):
+        q = wl.step_query(sh, k, DEV, w.seed)
+        o0, l0 = ops.stt_attn_fwd(q, Ks[: k + 1], Vs[: k + 1], T, sh.scale)
+        o0, l0 = o0.clone(), l0.clone()
+        for _ in range(12):
+            o, l = ops.stt_attn_fwd(q, Ks[: k + 1], Vs[: k + 1], T, sh.scale)
+            assert torch.equal(o.view(torch.int16), o0.view(torch.int16)), f"O differs, k={k}"
+            assert torch.equal(l.view(torch.int32), l0.view(torch.int32)), f"lse differs, k={k}"
+        assert ops.stt_device_error() == 0
+
+
 def test_tiny_workload_backward():
     """The tiny workload at the flat bound (2e-2 max-abs)."""
     w = wl.WORKLOADS["tiny"]
