@@ -59,7 +59,8 @@ struct BwdParams {
   float* dv0;
   float* delta;
   int B, H, H_kv, Q_LEN, k, n_t, G;
-  int head_chunk;           // heads per group of key-tile CTAs scheduled together
+  int g_sub;                // query heads per CTA (a divisor of G, all of one KV group)
+  int chunk_subs;           // head subgroups per group of CTAs scheduled together
   int accumulate;           // add into dK_j / dV_j, j >= 1 (read-modify-write)
   int zero_acc0;            // the prep kernel zeroes dk0 / dv0 first
   float scale, scale_log2;
@@ -437,21 +438,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float s_stat[2][2][kTile];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Heads are taken in chunks of P.head_chunk: the CTAs of one chunk run
+  // A CTA takes one key tile for g_sub query heads of one KV group (a head
+  // subgroup): the heads' query tiles run through one pipeline, head after
+  // head, and dK / dV accumulate over all of them in TMEM, so K and V are
+  // loaded once and the key tile's gradients leave once per subgroup.
+  // Subgroups are taken in chunks of P.chunk_subs: the CTAs of one chunk run
   // together and re-read only their heads' Q and dO, and add into only their
   // heads' dq, which stay in L2; within a chunk the key tiles go longest first.
-  const int nb = P.H * P.B;
-  const int ch = nb < P.head_chunk ? nb : P.head_chunk;
+  const int gs = P.g_sub;
+  const int subs_per_b = P.H / gs;
+  const int nsub = subs_per_b * P.B;
+  const int ch = nsub < P.chunk_subs ? nsub : P.chunk_subs;
   const int chunk = (int)(blockIdx.x / (unsigned)(P.n_t * ch));
-  const int chunk_heads = min(ch, nb - chunk * ch);
+  const int chunk_n = min(ch, nsub - chunk * ch);
   const int rem = (int)blockIdx.x - chunk * P.n_t * ch;
-  const int c = rem / chunk_heads;  // key tile; low tiles see the most query tiles
-  const int bh = chunk * ch + rem % chunk_heads;
-  const int b = bh / P.H, h = bh % P.H, hk = h / P.G;
+  const int c = rem / chunk_n;  // key tile; low tiles see the most query tiles
+  const int sg = chunk * ch + rem % chunk_n;
+  const int b = sg / subs_per_b;
+  const int bh0 = b * P.H + (sg - b * subs_per_b) * gs;  // first (b, h) of the subgroup
+  const int hk = (bh0 - b * P.H) / P.G;
   const int c0 = c * kTile;
   const int T = P.T[b];
-  const int t_first = c;                      // query tiles t >= c see this key tile
-  const int n_q = (c0 < T) ? (P.n_t - t_first) : 0;
+  const int t_first = c;                          // query tiles t >= c see this key tile
+  const int n_qh = (c0 < T) ? (P.n_t - t_first) : 0;  // query tiles per head
+  const int n_q = n_qh * gs;                      // tiles of the CTA, head-major
+  // Tile i: head bh0 + i / n_qh, query tile t_first + i % n_qh.
+  auto tile_bh = [&](int i) { return bh0 + i / n_qh; };
+  auto tile_q0 = [&](int i) { return (t_first + i % n_qh) * kTile; };
 
   if (tid == 0) {
     mbar_init(&bar_kv, 1);
@@ -506,14 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bar_q_full[st], L::kTileB);
         for (int cb = 0; cb < D / kColBlock; ++cb)
           tma_load_3d(smem + L::q0 + st * L::kTileB + cb * kTile * 128, &tmQ, &bar_q_full[st],
-                      cb * kColBlock, (t_first + i) * kTile, bh);
+                      cb * kColBlock, tile_q0(i), tile_bh(i));
       };
       auto load_do = [&](int i) {
         const int st = i % NS;
         mbar_arrive_expect_tx(&bar_do_full[st], L::kTileB);
         for (int cb = 0; cb < D / kColBlock; ++cb)
           tma_load_3d(smem + L::do0 + st * L::kTileB + cb * kTile * 128, &tmDO, &bar_do_full[st],
-                      cb * kColBlock, (t_first + i) * kTile, bh);
+                      cb * kColBlock, tile_q0(i), tile_bh(i));
       };
       int issued_q = 0, issued_do = 0;
       for (; issued_q < NS && issued_q < n_q; ++issued_q) {
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int i = 0; ok && i < n_q; ++i) {
         const int st = i % NS;
-        const int tq0 = (t_first + i) * kTile;
+        const int tq0 = tile_q0(i), tbh = tile_bh(i);
         const bool more = i + NS < n_q;
         // dQ of tile i, staged in its Q and dO buffers (dK(i) and dV(i) done).
         ok = mbar_wait(&bar_stg_full[i & 1], (uint32_t)(i >> 1) & 1u, STT_DEVERR_BWD_WAIT);
@@ -532,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Part A first; Q(i + NS) follows as soon as TMA has read it, ahead of
         // part B in TMA's queue, since S^T(i + NS) needs it first.
         for (int hh = 0; hh < 2; ++hh)
-          tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 0, hh, st), hh * (D / 2), tq0, bh);
+          tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 0, hh, st), hh * (D / 2), tq0, tbh);
         bulk_commit_group();
         bulk_wait_group_read0();
         if (more) {
@@ -541,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (NP == 2) {
           for (int hh = 0; hh < 2; ++hh)
-            tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 1, hh, st), hh * (D / 2) + 32, tq0, bh);
+            tma_reduce_add_3d(&tmDQ, dq_staging<D>(smem, 1, hh, st), hh * (D / 2) + 32, tq0, tbh);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
@@ -723,9 +736,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scaled only when it is stored.
     const int st_which = tid >> 7, st_idx = tid & 127;
     auto fetch_stat = [&](int i) -> float {
-      const int qq = (t_first + i) * kTile + st_idx;
+      const int qq = tile_q0(i) + st_idx;
       if (qq >= P.Q_LEN) return 0.f;
-      const size_t rq = (size_t)bh * P.Q_LEN + qq;
+      const size_t rq = (size_t)tile_bh(i) * P.Q_LEN + qq;
       return st_which == 0 ? P.lse[rq] : P.delta[rq];
     };
     auto put_stat = [&](int buf, float raw) {
@@ -742,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; ok && i < n_q; ++i) {
       const uint32_t par = (uint32_t)i & 1u;
-      const int tq0 = (t_first + i) * kTile;
+      const int tq0 = tile_q0(i);
       const int qh = tq0 + half * 64;  // first query of this thread's half
       // entry (kv, q) is visible iff kv < T, kv <= q and q < Q_LEN
       const bool full = kv_live && kv <= qh && qh + 64 <= P.Q_LEN;
@@ -974,9 +987,34 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   P.n_t = (a.Q_LEN + kTile - 1) / kTile;
   P.G = a.H / a.H_kv;
   {
+    // Heads per CTA: the largest divisor of G whose heaviest CTA (g_sub
+    // heads x n_t query tiles, key tile 0) stays within half of the average
+    // key-tile pairs per SM, so that the longest-first order still balances.
+    const int sms = sm_count();
+    long long pairs = 0;
+    for (int b = 0; b < a.B; ++b) {
+      const long long live = ((long long)a.T[b] + kTile - 1) / kTile;  // key tiles with c0 < T
+      pairs += live * P.n_t - live * (live - 1) / 2;
+    }
+    pairs *= a.H;
+    P.g_sub = 1;
+    for (int gsub = P.G; gsub > 1; --gsub)
+      if (P.G % gsub == 0 && 2LL * gsub * P.n_t * sms <= pairs) {
+        P.g_sub = gsub;
+        break;
+      }
+    // Subgroups per chunk: as many as keep their Q, dO (bf16) and dq (fp32) --
+    // 8 bytes per element -- within kChunkBytes of L2.  Even when a chunk is
+    // smaller than a wave of CTAs this order pays: a head's dq tiles take the
+    // reduce-adds of every key tile while they are still in L2 (one chunk
+    // spanning all heads made the varlen backward 18 % slower).
     const long long per_head = (long long)a.Q_LEN * D * 8;
-    long long ch = kChunkBytes / (per_head > 0 ? per_head : 1);
-    P.head_chunk = (int)(ch < 1 ? 1 : (ch > kHeadChunkMax ? kHeadChunkMax : ch));
+    long long heads = kChunkBytes / (per_head > 0 ? per_head : 1);
+    heads = heads < 1 ? 1 : (heads > kHeadChunkMax ? kHeadChunkMax : heads);
+    const long long nsub = (long long)a.B * a.H / P.g_sub;
+    long long cs = heads / P.g_sub;
+    if (cs < 1) cs = 1;
+    P.chunk_subs = (int)(cs > nsub ? nsub : cs);
   }
   P.scale = a.scale;
   P.scale_log2 = a.scale * kLog2e;
@@ -1008,7 +1046,7 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   prof_after(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  const unsigned grid = (unsigned)(P.n_t * a.H * a.B);
+  const unsigned grid = (unsigned)(P.n_t * (a.H / P.g_sub) * a.B);
   e = cudaFuncSetAttribute(attn_bwd_causal_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            CausalSmem<D>::alloc);
   if (e != cudaSuccess) return e;
