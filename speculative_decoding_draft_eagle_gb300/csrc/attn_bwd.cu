@@ -405,6 +405,46 @@ __device__ __forceinline__ unsigned char* dq_staging(unsigned char* smem, int p,
   return smem + (p == 0 ? q : o) + hh * L::kStageBlkB;
 }
 
+// P^T = 2^(S^T sl2 - lse2) for the 64 queries of one compute thread's half
+// (fp32 kept in pf for dS), written back as bf16 into the thread's own S^T
+// columns at tcol.  kMask: the tile holds masked entries (kv > q, kv >= T or
+// q >= Q_LEN), which get P = 0; full tiles take the body without the test.
+template <bool kMask>
+__device__ __forceinline__ void form_p(uint32_t (&pf)[2][32], const float* nlse_s, float sl2,
+                                       int qh, int kv, bool kv_live, int q_len, uint32_t tcol) {
+  const uint64_t sl2x2 = f32x2(sl2, sl2);
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t pp[16];
+#pragma unroll
+    for (int x4 = 0; x4 < 32; x4 += 4) {
+      // 2^(S sl2 - lse2), two queries per packed FMA
+      const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + c2 * 32 + x4);
+      float xv[4];
+      unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1])),
+                             sl2x2, f32x2(l4.x, l4.y)),
+                   xv[0], xv[1]);
+      unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3])),
+                             sl2x2, f32x2(l4.z, l4.w)),
+                   xv[2], xv[3]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float pv = ex2(xv[e]);
+        if constexpr (kMask) {
+          const int qa = qh + c2 * 32 + x4 + e;
+          if (!(kv_live && kv <= qa && qa < q_len)) pv = 0.f;
+        }
+        pf[c2][x4 + e] = __float_as_uint(pv);
+      }
+      pp[x4 >> 1] = pack_bf16(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1]));
+      pp[(x4 >> 1) + 1] =
+          pack_bf16(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3]));
+    }
+    // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
+    tmem_st16(tcol + c2 * 16, pp);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_causal_kernel(const __grid_constant__ BwdParams P,
@@ -770,37 +810,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pf[2][32];
       tmem_ld32x2(tmem + lane_off + kColS + half * 64, tmem + lane_off + kColS + half * 64 + 32,
                   pf[0], pf[1]);
-      const uint64_t sl2x2 = f32x2(sl2, sl2);
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pp[16];
-#pragma unroll
-        for (int x4 = 0; x4 < 32; x4 += 4) {
-          // 2^(S sl2 - lse2), two queries per packed FMA
-          const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + c2 * 32 + x4);
-          float xv[4];
-          unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1])),
-                                 sl2x2, f32x2(l4.x, l4.y)),
-                       xv[0], xv[1]);
-          unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3])),
-                                 sl2x2, f32x2(l4.z, l4.w)),
-                       xv[2], xv[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pv = ex2(xv[e]);
-            if (!full) {
-              const int qa = qh + c2 * 32 + x4 + e;
-              if (!(kv_live && kv <= qa && qa < P.Q_LEN)) pv = 0.f;
-            }
-            pf[c2][x4 + e] = __float_as_uint(pv);
-          }
-          pp[x4 >> 1] = pack_bf16(__uint_as_float(pf[c2][x4]), __uint_as_float(pf[c2][x4 + 1]));
-          pp[(x4 >> 1) + 1] =
-              pack_bf16(__uint_as_float(pf[c2][x4 + 2]), __uint_as_float(pf[c2][x4 + 3]));
-        }
-        // P^T of queries [qh + 32 c2, +32) into this half's own S^T columns.
-        tmem_st16(tmem + lane_off + kColS + half * 64 + c2 * 16, pp);
-      }
+      // The choice of body must be warp-uniform: form_p ends in a warp-wide
+      // TMEM store (tcgen05.st .sync.aligned), which every lane of the warp
+      // has to reach through the same instruction.
+      const uint32_t tcol = tmem + lane_off + kColS + half * 64;
+      if (__all_sync(0xffffffffu, full))
+        form_p<false>(pf, nlse_s, sl2, qh, kv, kv_live, P.Q_LEN, tcol);
+      else
+        form_p<true>(pf, nlse_s, sl2, qh, kv, kv_live, P.Q_LEN, tcol);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bar_p_ready);
