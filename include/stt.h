@@ -134,7 +134,8 @@ STT_API int stt_debug_inject(uint32_t what);
  *  D        head dimension, 64 or 128.
  *  Q_LEN    block length, >= 1.
  *  k        TTT step, 0 <= k <= STT_MAX_STEP.
- *  scale    softmax scale applied to q.K (1/sqrt(D) in the usual case).
+ *  scale    softmax scale applied to q.K (1/sqrt(D) in the usual case); finite
+ *           and > 0 (STT_ERR_INVALID_ARG otherwise).
  *  out      bf16 [B, H, Q_LEN, D]: O = softmax(scale q Kc^T + mask) Vc,
  *           rounded to nearest even.  A row with no visible key (T[b] = 0)
  *           is written as zeros.

@@ -64,6 +64,8 @@ struct BwdParams {
   int accumulate;           // add into dK_j / dV_j, j >= 1 (read-modify-write)
   int zero_acc0;            // the prep kernel zeroes dk0 / dv0 first
   float scale, scale_log2;
+  float log2_scale;         // log2(scale): folds scale into P in the causal kernel
+  float inv_scale;
   int T[kMaxBatch];
 };
 
@@ -724,12 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // dQ comes out of TMEM already scaled (dS carries the scale).
     auto stage = [&](unsigned char* blk, const uint32_t (&u)[32]) {
 #pragma unroll
       for (int w = 0; w < 8; ++w)
-        *reinterpret_cast<float4*>(blk + swz128(r, w)) = make_float4(
-            P.scale * __uint_as_float(u[4 * w]), P.scale * __uint_as_float(u[4 * w + 1]),
-            P.scale * __uint_as_float(u[4 * w + 2]), P.scale * __uint_as_float(u[4 * w + 3]));
+        *reinterpret_cast<float4*>(blk + swz128(r, w)) =
+            make_float4(__uint_as_float(u[4 * w]), __uint_as_float(u[4 * w + 1]),
+                        __uint_as_float(u[4 * w + 2]), __uint_as_float(u[4 * w + 3]));
     };
     bool ok = true;
     for (int i = 0; ok && i < n_q; ++i) {
@@ -782,7 +785,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return st_which == 0 ? P.lse[rq] : P.delta[rq];
     };
     auto put_stat = [&](int buf, float raw) {
-      s_stat[buf][st_which][st_idx] = st_which == 0 ? -raw * kLog2e : -raw;
+      // P is formed as scale * 2^(S sl2 - lse2) = 2^(S sl2 - lse2 + log2 scale):
+      // dS, dQ and dK then carry the attention scale with no multiply of their
+      // own, and dV (P^T dO) comes out scaled once, undone at the end.
+      s_stat[buf][st_which][st_idx] = st_which == 0 ? -raw * kLog2e + P.log2_scale : -raw;
     };
     uint32_t grp_uses = 0;
     bool ok = true;
@@ -887,12 +893,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
             const uint32_t o = swz128(r, w);
-            *reinterpret_cast<float4*>(bv + o) =
-                make_float4(__uint_as_float(uv[4 * w]), __uint_as_float(uv[4 * w + 1]),
-                            __uint_as_float(uv[4 * w + 2]), __uint_as_float(uv[4 * w + 3]));
-            *reinterpret_cast<float4*>(bk + o) = make_float4(
-                P.scale * __uint_as_float(uk[4 * w]), P.scale * __uint_as_float(uk[4 * w + 1]),
-                P.scale * __uint_as_float(uk[4 * w + 2]), P.scale * __uint_as_float(uk[4 * w + 3]));
+            *reinterpret_cast<float4*>(bv + o) = make_float4(
+                P.inv_scale * __uint_as_float(uv[4 * w]), P.inv_scale * __uint_as_float(uv[4 * w + 1]),
+                P.inv_scale * __uint_as_float(uv[4 * w + 2]),
+                P.inv_scale * __uint_as_float(uv[4 * w + 3]));
+            *reinterpret_cast<float4*>(bk + o) =
+                make_float4(__uint_as_float(uk[4 * w]), __uint_as_float(uk[4 * w + 1]),
+                            __uint_as_float(uk[4 * w + 2]), __uint_as_float(uk[4 * w + 3]));
           }
         }
         fence_proxy_async_smem();
@@ -1035,6 +1042,8 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   }
   P.scale = a.scale;
   P.scale_log2 = a.scale * kLog2e;
+  P.log2_scale = log2f(a.scale);
+  P.inv_scale = 1.0f / a.scale;
   for (int b = 0; b < a.B; ++b) P.T[b] = a.T[b];
 
   CUtensorMap tmQ, tmDO, tmK, tmV;

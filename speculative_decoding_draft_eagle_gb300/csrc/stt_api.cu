@@ -89,7 +89,7 @@ int check_attn(const void* q, const void* const* k_blocks, const void* const* v_
   if (B < 1 || B > STT_MAX_BATCH || H < 1 || H_kv < 1 || Q_LEN < 1) return STT_ERR_INVALID_ARG;
   if (H % H_kv != 0) return STT_ERR_INVALID_ARG;
   if (k < 0 || k > STT_MAX_STEP) return STT_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return STT_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return STT_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return STT_ERR_UNSUPPORTED;
   if (H / H_kv > 8) return STT_ERR_UNSUPPORTED;
   if ((long long)B * H * Q_LEN > (1ll << 31) - 1) return STT_ERR_UNSUPPORTED;

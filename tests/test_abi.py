@@ -70,6 +70,8 @@ def test_attn_fwd_rejects_bad_arguments(L):
     assert call(kb=_ptrs([good, good + 4])) == -3
     assert call(kb=_ptrs([good, 0])) == -1
     assert call(s=float("nan")) == -1
+    assert call(s=0.0) == -1               # the kernels need scale > 0
+    assert call(s=-0.1) == -1
     assert call(out=None) == -1
     assert call(H=64, Hkv=4) == -2         # group of 16 query heads: unsupported
 
