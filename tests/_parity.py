@@ -37,6 +37,12 @@ FWD_CASES = [
     (1, 6, 2, 256, 128, 2, [200]),         # group of 3 (below the unrolled bound of 4)
     (1, 6, 1, 192, 128, 5, [150]),         # group of 6 (below the unrolled bound of 8)
     (1, 3, 1, 129, 64, 2, [100]),          # odd row count: a partly filled last warp
+    # More work items than SMs: each persistent forward CTA walks several query
+    # tiles (Q buffers reused, barrier phases carried across items), including
+    # items of empty sequences (T = 0: no key tiles, zero O) next to full ones;
+    # the backward takes two query heads per CTA here (1536 key-tile pairs).
+    (48, 16, 4, 256, 128, 1, [256, 0, 1, 129, 200, 256, 77, 0] * 6),
+    (4, 12, 3, 512, 64, 2, [512, 0, 77, 300]),  # D = 64, 192 forward items
 ]
 
 
@@ -190,8 +196,10 @@ def emulated_backward(q, K_blocks, V_blocks, T, scale, dO, rounding=True):
     """dq, dK, dV of the sparse-tree attention in fp64, repeating the GPU path's
     roundings when ``rounding`` is set:
       * O is stored in bf16, and Delta = rowsum(dO * O) is taken from it;
-      * in block 0 (the tensor-core part) P enters dV = P^T dO as bf16, and
-        dS = P (dP - Delta) enters dK = scale dS^T q and dq = scale dS K as bf16;
+      * in block 0 (the tensor-core part) the kernel carries the attention
+        scale in P: scale P enters dV = (scale P)^T dO / scale as bf16, and
+        scale dS = scale P (dP - Delta) enters dK = (scale dS)^T q and
+        dq = (scale dS) K as bf16;
       * the suffix keys (blocks j >= 1) are computed without operand rounding.
     With ``rounding`` off it is the exact backward.  Inputs as the oracle's
     ``backward`` (q [B,H,Q,D], K/V blocks [B,H_kv,Q,D]); dense mask."""
@@ -227,11 +235,11 @@ def emulated_backward(q, K_blocks, V_blocks, T, scale, dO, rounding=True):
             dS = P * (dP - delta[:, None])
             causal = np.zeros(M.shape, dtype=bool)
             causal[:, :Q] = True
-            Pm = np.where(causal, rb(P), P)
-            dSm = np.where(causal, rb(dS), dS)
-            dq[b, h] = scale * dSm @ Kc
-            dKc = scale * dSm.T @ q[b, h]
-            dVc = Pm.T @ dO[b, h]
+            Pm = np.where(causal, rb(scale * P), scale * P)
+            dSm = np.where(causal, rb(scale * dS), scale * dS)
+            dq[b, h] = dSm @ Kc
+            dKc = dSm.T @ q[b, h]
+            dVc = Pm.T @ dO[b, h] / scale
             for j in range(k + 1):
                 dK[j][b, g] += dKc[j * Q:(j + 1) * Q]
                 dV[j][b, g] += dVc[j * Q:(j + 1) * Q]
