@@ -13,19 +13,22 @@
 //      (q < T, blocks j = 1..k: one key per query, so dK_j / dV_j row q is owned
 //      by this warp and written directly); dq initialised with the suffix part;
 //      dK_0 / dV_0 zeroed for the causal kernel's accumulation.
-//   2. causal (tcgen05, one CTA per 128-row key tile of a query head, looping
-//      over the query tiles that see it): S^T = K Q^T and dP^T = V dO^T in
+//   2. causal (tcgen05, one CTA per 128-row key tile of a subgroup of the
+//      query heads of one KV group, looping over the heads' query tiles that
+//      see it, head after head): S^T = K Q^T and dP^T = V dO^T in
 //      TMEM; 8 compute warps form P^T (written back into TMEM as bf16), then
 //      dS^T (written to shared memory as bf16); dV += P^T dO (A from TMEM),
 //      dK += dS^T Q and dQ = dS K (A = the dS^T tile read MN-major, i.e.
 //      transposed) run on the tensor cores.  The MMA warp issues S^T(i+1)
 //      right after dV(i), so it runs while the compute warps form dS(i).  dV
-//      and dK stay in TMEM across the query tiles.  Each tile's dQ is read out
+//      and dK stay in TMEM across the query tiles of all the subgroup's heads.
+//      P^T is formed by a warp-uniform choice of a body with or without the
+//      visibility test, and carries the attention scale (so dS, dQ and dK do).
+//      Each tile's dQ is read out
 //      of TMEM, staged in shared memory and added to the fp32 dq by TMA
 //      reduce-add (issued by the producer warp, which releases each staging
 //      buffer as soon as TMA has read it); the final dK / dV of the key tile
-//      are reduce-added the same way into dK_0 / dV_0, summing the group's
-//      query heads.
+//      are reduce-added the same way into dK_0 / dV_0, once per subgroup.
 // Every causal score entry costs 5 tensor-core products (the useful 10*D
 // flops); dq, dK_0 and dV_0 receive their partial sums in arrival order.
 #include "../../include/stt.h"
