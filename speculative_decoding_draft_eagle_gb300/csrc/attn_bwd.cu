@@ -1014,22 +1014,35 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
   P.n_t = (a.Q_LEN + kTile - 1) / kTile;
   P.G = a.H / a.H_kv;
   {
-    // Heads per CTA: the largest divisor of G whose heaviest CTA (g_sub
-    // heads x n_t query tiles, key tile 0) stays within half of the average
-    // key-tile pairs per SM, so that the longest-first order still balances.
+    // Heads per CTA: the divisor g of G that minimises an estimate of the
+    // busiest SM's work, in units of one (key tile, query tile) pair: the
+    // mean load (every pair, plus kCtaFixedPairs per CTA that has work) plus
+    // kTailShare of the heaviest CTA (g n_t pairs and its fixed cost), which
+    // the longest-first order leaves partly unbalanced at the end.  More
+    // heads per CTA pay the fixed cost (K/V load, first tile, final dK / dV)
+    // less often but make the heaviest CTAs longer.
+    constexpr double kCtaFixedPairs = 3.7;  // ~9.2 us of set-up and tail against ~2.5 us per pair
+    constexpr double kTailShare = 0.2;      // from a simulation of the longest-first dispatch
     const int sms = sm_count();
-    long long pairs = 0;
+    long long pairs = 0, live_tiles = 0;
     for (int b = 0; b < a.B; ++b) {
       const long long live = ((long long)a.T[b] + kTile - 1) / kTile;  // key tiles with c0 < T
       pairs += live * P.n_t - live * (live - 1) / 2;
+      live_tiles += live;
     }
     pairs *= a.H;
     P.g_sub = 1;
-    for (int gsub = P.G; gsub > 1; --gsub)
-      if (P.G % gsub == 0 && 2LL * gsub * P.n_t * sms <= pairs) {
+    double best = 0.0;
+    for (int gsub = 1; gsub <= P.G; ++gsub) {
+      if (P.G % gsub != 0) continue;
+      const double ctas = (double)live_tiles * (a.H / gsub);
+      const double est = ((double)pairs + ctas * kCtaFixedPairs) / sms +
+                         kTailShare * ((double)gsub * P.n_t + kCtaFixedPairs);
+      if (gsub == 1 || est < best) {
+        best = est;
         P.g_sub = gsub;
-        break;
       }
+    }
     // Subgroups per chunk: as many as keep their Q, dO (bf16) and dq (fp32) --
     // 8 bytes per element -- within kChunkBytes of L2.  Even when a chunk is
     // smaller than a wave of CTAs this order pays: a head's dq tiles take the
