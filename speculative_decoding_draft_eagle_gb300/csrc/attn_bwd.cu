@@ -100,111 +100,29 @@ __device__ __forceinline__ float group_sum(float v) {
   return v;
 }
 
-// E consecutive bf16 values (E = 4 or 8) packed in pairs: one 8- or 16-byte access.
-template <int E>
-struct Bf16Vec {
-  uint32_t w[E / 2];
-};
-
-template <int E>
-__device__ __forceinline__ Bf16Vec<E> ldg_vec(const __nv_bfloat16* p) {
-  Bf16Vec<E> v;
-  if constexpr (E == 8) {
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(p));
-    v.w[0] = x.x;
-    v.w[1] = x.y;
-    v.w[2] = x.z;
-    v.w[3] = x.w;
-  } else {
-    const uint2 x = __ldg(reinterpret_cast<const uint2*>(p));
-    v.w[0] = x.x;
-    v.w[1] = x.y;
-  }
-  return v;
-}
-
-template <int E>
-__device__ __forceinline__ Bf16Vec<E> zero_vec() {
-  Bf16Vec<E> v;
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) v.w[i] = 0u;
-  return v;
-}
-
-// Dot product of two packed bf16 vectors (fp32 accumulate).
-template <int E>
-__device__ __forceinline__ float dot_vec(const Bf16Vec<E>& a, const Bf16Vec<E>& b) {
-  float x = 0.f, y = 0.f;
-#pragma unroll
-  for (int i = 0; i < E / 2; ++i) {
-    x = fmaf(bf16lo(a.w[i]), bf16lo(b.w[i]), x);
-    y = fmaf(bf16hi(a.w[i]), bf16hi(b.w[i]), y);
-  }
-  return x + y;
-}
-
-// Element e of a packed bf16 vector as fp32.
-template <int E>
-__device__ __forceinline__ float vec_at(const Bf16Vec<E>& a, int e) {
-  return (e & 1) ? bf16hi(a.w[e >> 1]) : bf16lo(a.w[e >> 1]);
-}
-
-// E fp32 values to 4E aligned bytes; `stream` marks lines nothing reads again.
-template <int E>
-__device__ __forceinline__ void store_vec(float* p, const float (&v)[E], bool stream) {
-  float4* p4 = reinterpret_cast<float4*>(p);
-#pragma unroll
-  for (int i = 0; i < E / 4; ++i) {
-    const float4 x = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    if (stream)
-      __stcs(p4 + i, x);
-    else
-      p4[i] = x;
-  }
-}
-
-// E fp32 values of a gradient row into fp32 (OUT = float) or bf16 (OUT =
-// __nv_bfloat16, rounded to nearest even) memory at `p`; with `acc` the values
-// are added to what is there (in fp32, then rounded once).
-template <typename OUT, int E>
-__device__ __forceinline__ void put_grad(void* base, size_t off, const float (&v)[E], bool acc) {
+// Four fp32 values of a gradient row into fp32 (OUT = float) or bf16 (OUT =
+// __nv_bfloat16, rounded to nearest even) memory at element `off` of `base`;
+// with `acc` they are added to what is there (in fp32, then rounded once).
+// Overwritten rows go out with streaming stores: this kernel never reads them.
+template <typename OUT>
+__device__ __forceinline__ void put_grad4(void* base, size_t off, const float* v, bool acc) {
   if constexpr (sizeof(OUT) == 4) {
-    float* p = static_cast<float*>(base) + off;
-    if (!acc) {
-      store_vec<E>(p, v, true);
-      return;
-    }
-    float4* p4 = reinterpret_cast<float4*>(p);
-#pragma unroll
-    for (int i = 0; i < E / 4; ++i) {
-      float4 x = p4[i];
-      x.x += v[4 * i];
-      x.y += v[4 * i + 1];
-      x.z += v[4 * i + 2];
-      x.w += v[4 * i + 3];
-      p4[i] = x;
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+    if (acc) {
+      const float4 x = *p;
+      *p = make_float4(x.x + v[0], x.y + v[1], x.z + v[2], x.w + v[3]);
+    } else {
+      __stcs(p, make_float4(v[0], v[1], v[2], v[3]));
     }
   } else {
-    static_assert(E == 8, "bf16 gradient rows are written 16 bytes at a time");
-    uint4* p4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
-    float w[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) w[e] = v[e];
+    uint2* p = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(base) + off);
     if (acc) {
-      const uint4 x = *p4;
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[2 * i] += bf16lo(xs[i]);
-        w[2 * i + 1] += bf16hi(xs[i]);
-      }
+      const uint2 x = *p;
+      *p = make_uint2(pack_bf16(bf16lo(x.x) + v[0], bf16hi(x.x) + v[1]),
+                      pack_bf16(bf16lo(x.y) + v[2], bf16hi(x.y) + v[3]));
+    } else {
+      __stcs(p, make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3])));
     }
-    const uint4 y = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]),
-                               pack_bf16(w[6], w[7]));
-    if (acc)
-      *p4 = y;
-    else
-      __stcs(p4, y);
   }
 }
 
@@ -214,152 +132,324 @@ __device__ __forceinline__ uint32_t swz128(int r, int w) {
 }
 
 // ------------------------------------------------------------------ prep --
-// A group of L = D/E lanes owns one (b, KV head, row q); lane l of the group
-// holds elements [E l, E l + E) of every row it touches, so a warp covers 32/L
-// consecutive (contiguous) rows.  GM is the compile-time bound of the group
-// size (the loops over heads are unrolled so per-head values stay in
-// registers); G <= GM.
-// Register budget per group size: the per-head q, dO and dq values grow with
-// the heads a thread holds, so larger groups run fewer, fatter warps per SM.
-// Groups of eight split their heads between the two half-warps (SH = 2): each
-// thread holds four heads, the half-warps combine their dK_j / dV_j partial
-// sums with one shuffle, and a warp covers half as many rows.
-template <int GM>
-struct PrepShape {
-  static constexpr int E = 8;                               // 16-byte accesses
-  static constexpr int SH = GM >= 8 ? 2 : 1;                // half-warps sharing a row's heads
-  static constexpr int GH = GM / SH;                        // heads per thread
-  static constexpr int kJ = GH <= 2 ? 4 : 2;                // suffix blocks loaded together
-  static constexpr int kThreads = GH <= 2 ? 256 : 128;
-  static constexpr int kMinBlocks = GH <= 2 ? 2 : 3;
+// The prep kernel streams: per (b, KV head, row q) it reads the O, dO (and,
+// with suffix keys, q) rows of the group's query heads and the K_j, V_j rows,
+// and writes Delta, dq, dK_j, dV_j (and zeroed dK_0 / dV_0 rows); a handful
+// of flops per byte.  Units of R consecutive rows q0.. of one (b, KV head) are
+// dealt round robin to one CTA per SM.  Warp kComputeWarps (one lane) copies
+// each unit into a ring of shared-memory slots, one [rows x D] bf16 block per
+// slot and bulk copy, as far ahead as the ring reaches (176 KB per SM in
+// flight), in groups that complete on one mbarrier: the O and dO blocks of
+// the group's heads; when the unit has rows q < T and k > 0, their q blocks;
+// then K_j with V_j for j = 1..k (rows q < T only).  The compute warps take
+// each unit together and give a slot back as soon as every warp has read it
+// into registers.  L = D/8 lanes serve one (row, head half); lane l holds
+// elements [4l, 4l + 4) and [D/2 + 4l, +4) of the row as fp32 pairs (packed
+// f32x2 arithmetic), so each 16-byte fp32 store of a lane group writes 2D
+// contiguous bytes.  Groups of eight heads are split between two lane groups
+// per row (SH = 2), which add their dK_j / dV_j partial sums with one shuffle.
+// GM is the compile-time bound of the group size; head slots past G hold zeros.
+template <int D, int GM>
+struct PrepCfg {
+  static constexpr int L = D / 8;                // lanes per (row, head half)
+  static constexpr int SH = GM >= 8 ? 2 : 1;     // lane groups sharing a row's heads
+  static constexpr int GH = GM / SH;             // head slots per thread
+  // Twelve warps in all, three per SM sub-partition, so that a thread may
+  // hold up to 168 registers (four warps per sub-partition would cap it at
+  // 128 and spill the per-head values).
+  static constexpr int kComputeWarps = 11;
+  static constexpr int kCompute = kComputeWarps * 32;
+  static constexpr int kThreads = kCompute + 32;  // + the copy warp
+  static constexpr int R = kCompute / (L * SH);  // query rows per unit
+  static constexpr int kSlotB = R * D * 2;       // one [R x D] bf16 block (5.5 KB / SH)
+  static constexpr int kLogSlots = SH == 1 ? 5 : 6;
+  static constexpr int kSlots = 1 << kLogSlots;  // 176 KB of slots
+  static constexpr int kSmem = kSlots * kSlotB;
+  static_assert(2 * GM <= kSlots, "a unit's O and dO blocks fit in the ring at once");
+  static_assert(kSlotB % 16 == 0 && (D * 2) % 16 == 0, "bulk copies move 16-byte multiples");
 };
 
-template <int D, int GM, typename OUT>
-__global__ void __launch_bounds__(PrepShape<GM>::kThreads, PrepShape<GM>::kMinBlocks)
-    attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
-  constexpr int E = PrepShape<GM>::E;
-  constexpr int SH = PrepShape<GM>::SH;
-  constexpr int GH = PrepShape<GM>::GH;
-  constexpr int kJ = PrepShape<GM>::kJ;
-  constexpr int L = D / E;            // lanes per row
-  constexpr int RPW = 32 / SH / L;    // rows per warp
-  constexpr int kWarps = PrepShape<GM>::kThreads / 32;
-  using V = Bf16Vec<E>;
-  const int lane = threadIdx.x & 31;
-  const int hh = lane / (32 / SH);    // which heads of the group: [hh GH, hh GH + GH)
-  const int lane_h = lane % (32 / SH);
-  const int sub = lane_h / L, li = lane_h % L;
-  const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
-  const long long stride = (long long)gridDim.x * kWarps * RPW;
-  const int G = P.G;
-  for (long long base = ((long long)blockIdx.x * kWarps + (threadIdx.x >> 5)) * RPW; base < rows;
-       base += stride) {
-    // Every lane stays in the loop body (the group sums shuffle across the
-    // warp); lanes past the last row only skip their memory accesses.
-    const long long row = base + sub;
-    const bool live = row < rows;
-    const int q = live ? (int)(row % P.Q_LEN) : 0;
-    const int bhk = live ? (int)(row / P.Q_LEN) : 0;
-    const int b = bhk / P.H_kv, hk = bhk % P.H_kv;
-    const bool valid = live && q < P.T[b];  // rows with suffix keys
-    const size_t kvoff = ((size_t)bhk * P.Q_LEN + q) * D + li * E;
+// Elements [4l, 4l + 4) and [D/2 + 4l, D/2 + 4l + 4) of a bf16 row as four
+// fp32 pairs.
+template <int D>
+__device__ __forceinline__ void lds_row8(const unsigned char* row, int l, uint64_t (&v)[4]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(row + 8 * l);
+  const uint2 b = *reinterpret_cast<const uint2*>(row + D + 8 * l);
+  v[0] = f32x2(bf16lo(a.x), bf16hi(a.x));
+  v[1] = f32x2(bf16lo(a.y), bf16hi(a.y));
+  v[2] = f32x2(bf16lo(b.x), bf16hi(b.x));
+  v[3] = f32x2(bf16lo(b.y), bf16hi(b.y));
+}
 
-    V qv[GH], dov[GH];
-    float dq[GH][E], lse2[GH], dl[GH];
-    {
-      V ov[GH];
-#pragma unroll
-      for (int i = 0; i < GH; ++i) {
-        qv[i] = dov[i] = ov[i] = zero_vec<E>();
-        lse2[i] = 0.f;
-        if (hh * GH + i < G && live) {
-          const size_t rq = (size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q;
-          const size_t off = rq * D + li * E;
-          dov[i] = ldg_vec<E>(P.dout + off);
-          ov[i] = ldg_vec<E>(P.out + off);
-          if (valid && P.k > 0) qv[i] = ldg_vec<E>(P.q + off);
-          lse2[i] = P.lse[rq] * kLog2e;
-        }
-      }
-      // The group sums shuffle across the whole warp, so every lane runs them
-      // for every head slot; slots past the group's heads hold zeros and add
-      // nothing.
-#pragma unroll
-      for (int i = 0; i < GH; ++i) {
-        dl[i] = group_sum<L>(dot_vec<E>(dov[i], ov[i]));
-        if (hh * GH + i < G && live && li == 0)
-          P.delta[(size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q] = dl[i];
-#pragma unroll
-        for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
-      }
+// Sum of the four pair products a[m] b[m] (both halves).
+__device__ __forceinline__ float dot_pairs(const uint64_t (&a)[4], const uint64_t (&b)[4]) {
+  uint64_t acc = mul_f32x2(a[0], b[0]);
+  acc = fma_f32x2(a[1], b[1], acc);
+  acc = fma_f32x2(a[2], b[2], acc);
+  acc = fma_f32x2(a[3], b[3], acc);
+  float lo, hi;
+  unpack_f32x2(acc, lo, hi);
+  return lo + hi;
+}
+
+template <int D, int GM, typename OUT>
+__global__ void __launch_bounds__(PrepCfg<D, GM>::kThreads, 1)
+    attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
+  using C = PrepCfg<D, GM>;
+  constexpr int L = C::L, SH = C::SH, GH = C::GH, R = C::R, NS = C::kSlots, LNS = C::kLogSlots;
+  extern __shared__ __align__(128) unsigned char prep_smem[];
+  __shared__ uint64_t bar_full[NS], bar_empty[NS];
+  if ((smem_u32(prep_smem) & 15u) != 0) {
+    if (threadIdx.x == 0) record_error(STT_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G;
+  const int n_qb = (P.Q_LEN + R - 1) / R;
+  const long long n_units = (long long)P.B * P.H_kv * n_qb;
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], C::kComputeWarps);
     }
-    // Blocks are taken kJ at a time with all their row loads issued up front.
-    for (int j0 = 1; j0 <= P.k; j0 += kJ) {
-      V kv[kJ], vv[kJ];
-#pragma unroll
-      for (int u = 0; u < kJ; ++u) {
-        kv[u] = vv[u] = zero_vec<E>();
-        if (valid && j0 + u <= P.k) {
-          kv[u] = ldg_vec<E>(P.kb[j0 + u] + kvoff);
-          vv[u] = ldg_vec<E>(P.vb[j0 + u] + kvoff);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Unit u: rows [q0, q0 + R) of (b, KV head hk); nrows of them exist
+  // (q < Q_LEN) and the first nv have suffix keys (q < T, k > 0).
+  struct Unit {
+    int b, hk, q0, nrows, nv;
+  };
+  auto unit_at = [&](long long u) {
+    Unit x;
+    const long long bhk = u / n_qb;
+    x.q0 = (int)(u - bhk * n_qb) * R;
+    x.b = (int)(bhk / P.H_kv);
+    x.hk = (int)(bhk - (long long)x.b * P.H_kv);
+    x.nrows = min(R, P.Q_LEN - x.q0);
+    const int T = P.T[x.b];
+    x.nv = (P.k > 0 && x.q0 < T) ? min(R, T - x.q0) : 0;
+    return x;
+  };
+
+  if (warp == C::kComputeWarps) {
+    // ------------------------------------------------------------- copies --
+    if (lane == 0) {
+      uint32_t seq = 0;  // slots filled so far; slot seq % NS, use seq / NS
+      bool ok = true;
+      // Slots [seq, seq + cnt) take cnt blocks of `rows` rows (src(c) for
+      // block c); all their bytes complete on the first slot's barrier, whose
+      // phase the compute warps wait for; the others' phases are completed
+      // at once so that every slot's barrier keeps one phase per use.
+      auto put_group = [&](int cnt, int rows, auto src) {
+        for (int c = 0; ok && c < cnt; ++c) {
+          const uint32_t n = seq + c;
+          if (n >= (uint32_t)NS)
+            ok = mbar_wait(&bar_empty[n & (NS - 1)], ((n >> LNS) - 1u) & 1u, STT_DEVERR_BWD_WAIT);
+        }
+        if (!ok) return;
+        const uint32_t bytes = (uint32_t)rows * D * 2;
+        uint64_t* bar = &bar_full[seq & (NS - 1)];
+        mbar_arrive_expect_tx(bar, bytes * cnt);
+        for (int c = 1; c < cnt; ++c) mbar_arrive(&bar_full[(seq + c) & (NS - 1)]);
+        for (int c = 0; c < cnt; ++c)
+          bulk_load(prep_smem + (size_t)((seq + c) & (NS - 1)) * C::kSlotB, src(c), bytes, bar);
+        seq += cnt;
+      };
+      for (long long u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const Unit x = unit_at(u);
+        // row q0 of query head hk G of sequence b; head h is Q_LEN rows further
+        const size_t hq = ((size_t)x.b * P.H + (size_t)x.hk * G) * P.Q_LEN + x.q0;
+        put_group(2 * G, x.nrows, [&](int c) {
+          const __nv_bfloat16* t = c < G ? P.out : P.dout;
+          return t + (hq + (size_t)(c < G ? c : c - G) * P.Q_LEN) * D;
+        });
+        if (x.nv > 0) {
+          put_group(G, x.nv, [&](int c) { return P.q + (hq + (size_t)c * P.Q_LEN) * D; });
+          const size_t kvo = (((size_t)x.b * P.H_kv + x.hk) * P.Q_LEN + x.q0) * D;
+          for (int j = 1; ok && j <= P.k; ++j)
+            put_group(2, x.nv, [&](int c) { return (c == 0 ? P.kb[j] : P.vb[j]) + kvo; });
         }
       }
+      // Every copy issued lands before the CTA exits (on the normal path the
+      // compute warps have waited for all of them already): the last use of
+      // each slot is complete once its phase is.
+      for (uint32_t n = seq > (uint32_t)NS ? seq - NS : 0u; n < seq; ++n)
+        mbar_wait(&bar_full[n & (NS - 1)], (n >> LNS) & 1u, STT_DEVERR_BWD_WAIT);
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- compute --
+  const int r = tid / (L * SH), hh = (tid / L) % SH, l = tid % L;
+  const int e0 = 4 * l, e1 = D / 2 + 4 * l;  // this lane's two 4-element column groups
+  uint32_t seq = 0;
+  bool ok = true;
+  auto slot_row = [&](uint32_t n) -> const unsigned char* {
+    return prep_smem + (size_t)(n & (NS - 1)) * C::kSlotB + (size_t)r * D * 2;
+  };
+  // Waits for the group starting at slot n0; false (warp-uniform) on a give-up.
+  auto wait_group = [&](uint32_t n0) -> bool {
+    if (ok) ok = mbar_wait(&bar_full[n0 & (NS - 1)], (n0 >> LNS) & 1u, STT_DEVERR_BWD_WAIT);
+    ok = __all_sync(0xffffffffu, ok) != 0;
+    return ok;
+  };
+  // The warp gives slots [n0, n0 + cnt) back once all its lanes have read them.
+  auto release = [&](uint32_t n0, int cnt) {
+    __syncwarp();
+    if (lane == 0)
+      for (int c = 0; c < cnt; ++c) mbar_arrive(&bar_empty[(n0 + c) & (NS - 1)]);
+  };
+  // Four fp32 pairs (elements e0.. and e1..) of a gradient row.
+  auto put8 = [&](void* base, size_t row_off, const uint64_t (&v)[4], bool acc) {
+    float f[8];
 #pragma unroll
-      for (int u = 0; u < kJ; ++u) {
-        const int j = j0 + u;
-        if (j > P.k) break;
-        float dk[E], dv[E];
+    for (int m = 0; m < 4; ++m) unpack_f32x2(v[m], f[2 * m], f[2 * m + 1]);
+    put_grad4<OUT>(base, row_off + e0, f, acc);
+    put_grad4<OUT>(base, row_off + e1, f + 4, acc);
+  };
+
+  for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit x = unit_at(u);
+    const int q = x.q0 + r;
+    const bool live = r < x.nrows;  // q < Q_LEN
+    const bool valid = r < x.nv;    // q < T: the row has suffix keys
+    const size_t hq = ((size_t)x.b * P.H + (size_t)x.hk * G) * P.Q_LEN + q;  // head hk G, row q
+    const size_t kvr = (((size_t)x.b * P.H_kv + x.hk) * P.Q_LEN + q) * D;
+    float lse2[GH];
 #pragma unroll
-        for (int e = 0; e < E; ++e) dk[e] = dv[e] = 0.f;
+    for (int i = 0; i < GH; ++i) {
+      const int h = hh * GH + i;
+      // Rows without suffix keys never use it (their lse may be -inf).
+      lse2[i] = (h < G && valid) ? P.lse[hq + (size_t)h * P.Q_LEN] * kLog2e : 0.f;
+    }
+
+    // ---- Delta = sum_d dO O for every head; dO stays in registers.
+    uint64_t do2[GH][4];
+    float dl[GH];
+    if (!wait_group(seq)) break;
+#pragma unroll
+    for (int i = 0; i < GH; ++i) {
+      const int h = hh * GH + i;
+      uint64_t o2[4];
+      if (h < G && live) {
+        lds_row8<D>(slot_row(seq + h), l, o2);
+        lds_row8<D>(slot_row(seq + G + h), l, do2[i]);
+      } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) o2[m] = do2[i][m] = 0ull;
+      }
+      dl[i] = group_sum<L>(dot_pairs(do2[i], o2));
+      if (h < G && live && l == 0) P.delta[hq + (size_t)h * P.Q_LEN] = dl[i];
+    }
+    release(seq, 2 * G);
+    seq += 2 * G;
+
+    // ---- suffix keys: blocks j = 1..k, one key per query row.
+    uint64_t dq2[GH][4];
+#pragma unroll
+    for (int i = 0; i < GH; ++i)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) dq2[i][m] = 0ull;
+    // Rows without suffix keys get no contribution: written as zeros when the
+    // gradients are overwritten, left alone when they are accumulated.
+    const bool put = live && (valid || !P.accumulate);
+    if (x.nv > 0) {
+      uint64_t q2[GH][4];
+      if (!wait_group(seq)) break;
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        const int h = hh * GH + i;
+        if (h < G && valid) {
+          lds_row8<D>(slot_row(seq + h), l, q2[i]);
+        } else {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) q2[i][m] = 0ull;
+        }
+      }
+      release(seq, G);
+      seq += G;
+      for (int j = 1; j <= P.k; ++j) {
+        if (!wait_group(seq)) break;
+        uint64_t k2[4], v2[4];
+        if (valid) {
+          lds_row8<D>(slot_row(seq), l, k2);
+          lds_row8<D>(slot_row(seq + 1), l, v2);
+        } else {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) k2[m] = v2[m] = 0ull;
+        }
+        release(seq, 2);
+        seq += 2;
+        uint64_t dk2[4], dv2[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dk2[m] = dv2[m] = 0ull;
 #pragma unroll
         for (int i = 0; i < GH; ++i) {
-          // Head slots past the group's heads: qv = dov = 0 and Delta = 0, so
-          // dss = 0 and p dO = 0 (the sums still run on every lane).
-          const float s = group_sum<L>(dot_vec<E>(qv[i], kv[u]));
-          const float dp = group_sum<L>(dot_vec<E>(dov[i], vv[u]));
-          // Rows without suffix keys get no contribution (their lse may be -inf).
+          // Head slots past G: q = dO = 0 and Delta = 0, so dS = 0 and
+          // p dO = 0 (the sums still run on every lane).
+          const float s = group_sum<L>(dot_pairs(q2[i], k2));
+          const float dp = group_sum<L>(dot_pairs(do2[i], v2));
           const float p = valid ? ex2(s * P.scale_log2 - lse2[i]) : 0.f;
           const float dss = p * (dp - dl[i]) * P.scale;
+          const uint64_t dss2 = f32x2(dss, dss), p2 = f32x2(p, p);
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            dq[i][e] = fmaf(dss, vec_at<E>(kv[u], e), dq[i][e]);
-            dk[e] = fmaf(dss, vec_at<E>(qv[i], e), dk[e]);
-            dv[e] = fmaf(p, vec_at<E>(dov[i], e), dv[e]);
+          for (int m = 0; m < 4; ++m) {
+            dq2[i][m] = fma_f32x2(dss2, k2[m], dq2[i][m]);
+            dk2[m] = fma_f32x2(dss2, q2[i][m], dk2[m]);
+            dv2[m] = fma_f32x2(p2, do2[i][m], dv2[m]);
           }
         }
-        // Rows without suffix keys add nothing: written as zeros when the
-        // gradients are overwritten, left alone when they are accumulated.
-        const bool put = live && (valid || !P.accumulate);
         if constexpr (SH == 2) {
-          // The other half-warp holds the group's other heads: sum, then
-          // half-warp 0 stores dK_j and half-warp 1 dV_j.
+          // The other lane group of the row holds the other heads: add, then
+          // group 0 writes dK_j and group 1 dV_j.
+          uint64_t out[4];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            dk[e] += __shfl_xor_sync(0xffffffffu, dk[e], 16);
-            dv[e] += __shfl_xor_sync(0xffffffffu, dv[e], 16);
+          for (int m = 0; m < 4; ++m) {
+            const uint64_t ok2 = __shfl_xor_sync(0xffffffffu, dk2[m], L);
+            const uint64_t ov2 = __shfl_xor_sync(0xffffffffu, dv2[m], L);
+            out[m] = hh == 0 ? add_f32x2(dk2[m], ok2) : add_f32x2(dv2[m], ov2);
           }
-          float out[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) out[e] = hh == 0 ? dk[e] : dv[e];
-          if (put) put_grad<OUT, E>(hh == 0 ? P.dkb[j] : P.dvb[j], kvoff, out, P.accumulate != 0);
+          if (put) put8(hh == 0 ? P.dkb[j] : P.dvb[j], kvr, out, P.accumulate != 0);
         } else if (put) {
-          put_grad<OUT, E>(P.dkb[j], kvoff, dk, P.accumulate != 0);
-          put_grad<OUT, E>(P.dvb[j], kvoff, dv, P.accumulate != 0);
+          put8(P.dkb[j], kvr, dk2, P.accumulate != 0);
+          put8(P.dvb[j], kvr, dv2, P.accumulate != 0);
         }
+      }
+      if (!ok) break;
+    } else if (live && !P.accumulate) {
+      const uint64_t z[4] = {0ull, 0ull, 0ull, 0ull};
+      for (int j = 1; j <= P.k; ++j) {
+        if (SH == 1 || hh == 0) put8(P.dkb[j], kvr, z, false);
+        if (SH == 1 || hh == 1) put8(P.dvb[j], kvr, z, false);
       }
     }
     if (live) {
+      // dq starts as the suffix part; the causal kernel adds into it next, so
+      // these rows take ordinary (L2-allocating) stores.
 #pragma unroll
-      for (int i = 0; i < GH; ++i)
-        if (hh * GH + i < G)
-          store_vec<E>(P.dq + ((size_t)(b * P.H + hk * G + hh * GH + i) * P.Q_LEN + q) * D + li * E,
-                       dq[i], false);
+      for (int i = 0; i < GH; ++i) {
+        const int h = hh * GH + i;
+        if (h < G) {
+          float f[8];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) unpack_f32x2(dq2[i][m], f[2 * m], f[2 * m + 1]);
+          float* row = P.dq + (hq + (size_t)h * P.Q_LEN) * D;
+          *reinterpret_cast<float4*>(row + e0) = make_float4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<float4*>(row + e1) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
       if (P.zero_acc0) {
-        float z[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) z[e] = 0.f;
-        if (SH == 1 || hh == 0) store_vec<E>(P.dk0 + kvoff, z, false);
-        if (SH == 1 || hh == 1) store_vec<E>(P.dv0 + kvoff, z, false);
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (SH == 1 || hh == 0) {
+          *reinterpret_cast<float4*>(P.dk0 + kvr + e0) = z4;
+          *reinterpret_cast<float4*>(P.dk0 + kvr + e1) = z4;
+        }
+        if (SH == 1 || hh == 1) {
+          *reinterpret_cast<float4*>(P.dv0 + kvr + e0) = z4;
+          *reinterpret_cast<float4*>(P.dv0 + kvr + e1) = z4;
+        }
       }
     }
   }
@@ -963,16 +1053,17 @@ __global__ void __launch_bounds__(256) attn_bwd_cast_kernel(const __grid_constan
 }
 
 template <int D, int GM>
-void launch_prep(const BwdParams& P, bool bf16, cudaStream_t s) {
-  const long long rows = (long long)P.B * P.H_kv * P.Q_LEN;
-  using S = PrepShape<GM>;
-  const long long per_block = (S::kThreads / 32) * (32 / S::SH / (D / S::E));
-  long long blocks = (rows + per_block - 1) / per_block;
-  if (blocks > 152 * 64) blocks = 152 * 64;  // grid-stride beyond that
-  if (bf16)
-    attn_bwd_prep_kernel<D, GM, __nv_bfloat16><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
-  else
-    attn_bwd_prep_kernel<D, GM, float><<<(unsigned)blocks, S::kThreads, 0, s>>>(P);
+cudaError_t launch_prep(const BwdParams& P, bool bf16, cudaStream_t s) {
+  using C = PrepCfg<D, GM>;
+  const long long units = (long long)P.B * P.H_kv * ((P.Q_LEN + C::R - 1) / C::R);
+  const long long sms = sm_count();
+  const long long grid = units < sms ? units : sms;
+  if (grid <= 0) return cudaSuccess;
+  auto kern = bf16 ? attn_bwd_prep_kernel<D, GM, __nv_bfloat16> : attn_bwd_prep_kernel<D, GM, float>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, C::kThreads, C::kSmem, s>>>(P);
+  return cudaSuccess;
 }
 
 template <int D>
@@ -1078,14 +1169,15 @@ cudaError_t launch(const AttnArgs& a, const AttnBwdArgs& g, cudaStream_t s) {
 
   prof_before(s, STT_KERNEL_ATTN_BWD_PREP);
   if (P.G == 1)
-    launch_prep<D, 1>(P, bf16, s);
+    e = launch_prep<D, 1>(P, bf16, s);
   else if (P.G == 2)
-    launch_prep<D, 2>(P, bf16, s);
+    e = launch_prep<D, 2>(P, bf16, s);
   else if (P.G <= 4)
-    launch_prep<D, 4>(P, bf16, s);
+    e = launch_prep<D, 4>(P, bf16, s);
   else
-    launch_prep<D, 8>(P, bf16, s);
+    e = launch_prep<D, 8>(P, bf16, s);
   prof_after(s);
+  if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const unsigned grid = (unsigned)(P.n_t * (a.H / P.g_sub) * a.B);
