@@ -192,6 +192,51 @@ __device__ __forceinline__ float dot_pairs(const uint64_t (&a)[4], const uint64_
   return lo + hi;
 }
 
+// Sums of V values over the L lanes of an aligned lane group (V <= L, both
+// powers of two) by a reduce-scatter butterfly: at level t (offset L >> (t+1))
+// each lane keeps half of its current values, adding its partner's copy of
+// them, and sends the other half; after log2 V levels a lane holds one value
+// index, summed over the rest of the group by plain levels.  log2 V + log2 L
+// shuffles where one butterfly per value takes V log2 L.  Returns the total
+// of value scatter_index<L, V>(lane).
+template <int L, int V>
+__device__ __forceinline__ float reduce_scatter(float (&x)[V], int lane) {
+  constexpr int LV = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : 3;
+  static_assert(V == (1 << LV) && V <= L, "V: a power of two, at most L");
+#pragma unroll
+  for (int t = 0; t < LV; ++t) {
+    const int o = L >> (t + 1);
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int m = 0; m < (V >> (t + 1)); ++m) {
+      const float lo = x[m], hi = x[m + (V >> (t + 1))];
+      const float keep = up ? hi : lo, send = up ? lo : hi;
+      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float v = x[0];
+#pragma unroll
+  for (int o = L >> (LV + 1); o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// The value index whose total reduce_scatter<L, V> leaves in `lane`, and the
+// lane (within the group) that holds the total of value index v.
+template <int L, int V>
+__device__ __forceinline__ int scatter_index(int lane) {
+  int v = 0;
+#pragma unroll
+  for (int t = 0; (V >> (t + 1)) > 0; ++t)
+    if (lane & (L >> (t + 1))) v += V >> (t + 1);
+  return v;
+}
+template <int L, int V>
+__host__ __device__ constexpr int scatter_lane(int v) {
+  int l = 0;
+  for (int t = 0; (V >> (t + 1)) > 0; ++t)
+    if (v & (V >> (t + 1))) l += L >> (t + 1);
+  return l;
+}
+
 template <int D, int GM, typename OUT>
 __global__ void __launch_bounds__(PrepCfg<D, GM>::kThreads, 1)
     attn_bwd_prep_kernel(const __grid_constant__ BwdParams P) {
@@ -317,17 +362,22 @@ __global__ void __launch_bounds__(PrepCfg<D, GM>::kThreads, 1)
     const bool valid = r < x.nv;    // q < T: the row has suffix keys
     const size_t hq = ((size_t)x.b * P.H + (size_t)x.hk * G) * P.Q_LEN + q;  // head hk G, row q
     const size_t kvr = (((size_t)x.b * P.H_kv + x.hk) * P.Q_LEN + q) * D;
-    float lse2[GH];
-#pragma unroll
-    for (int i = 0; i < GH; ++i) {
-      const int h = hh * GH + i;
-      // Rows without suffix keys never use it (their lse may be -inf).
-      lse2[i] = (h < G && valid) ? P.lse[hq + (size_t)h * P.Q_LEN] * kLog2e : 0.f;
-    }
+    // Sums over a lane group are taken by reduce-scatter: the group's GH
+    // Delta partials leave lane l with the Delta of head slot i_me, and per
+    // suffix block its 2 GH partials (score and dP of each slot) leave it with
+    // one half of slot i_me's pair; it forms that head's p and dS, which the
+    // group then broadcasts.
+    constexpr int NV = 2 * GH;
+    constexpr int kPairOff = L >> (NV == 2 ? 1 : NV == 4 ? 2 : 3);  // lane holding the pair's other half
+    const int i_me = scatter_index<L, GH>(l);
+    const int h_me = hh * GH + i_me;
+    const bool my_dp = (scatter_index<L, NV>(l) & 1) != 0;  // this lane's half: score or dP
+    // Rows without suffix keys never use the lse (it may be -inf there).
+    const float my_lse2 = (h_me < G && valid) ? P.lse[hq + (size_t)h_me * P.Q_LEN] * kLog2e : 0.f;
 
     // ---- Delta = sum_d dO O for every head; dO stays in registers.
     uint64_t do2[GH][4];
-    float dl[GH];
+    float dpart[GH];
     if (!wait_group(seq)) break;
 #pragma unroll
     for (int i = 0; i < GH; ++i) {
@@ -340,11 +390,12 @@ __global__ void __launch_bounds__(PrepCfg<D, GM>::kThreads, 1)
 #pragma unroll
         for (int m = 0; m < 4; ++m) o2[m] = do2[i][m] = 0ull;
       }
-      dl[i] = group_sum<L>(dot_pairs(do2[i], o2));
-      if (h < G && live && l == 0) P.delta[hq + (size_t)h * P.Q_LEN] = dl[i];
+      dpart[i] = dot_pairs(do2[i], o2);
     }
     release(seq, 2 * G);
     seq += 2 * G;
+    const float my_dl = reduce_scatter<L, GH>(dpart, l);
+    if (h_me < G && live && l == scatter_lane<L, GH>(i_me)) P.delta[hq + (size_t)h_me * P.Q_LEN] = my_dl;
 
     // ---- suffix keys: blocks j = 1..k, one key per query row.
     uint64_t dq2[GH][4];
@@ -385,14 +436,23 @@ __global__ void __launch_bounds__(PrepCfg<D, GM>::kThreads, 1)
         uint64_t dk2[4], dv2[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) dk2[m] = dv2[m] = 0ull;
+        // Head slots past G: q = dO = 0 and Delta = 0, so dS = 0 and p dO = 0
+        // (the sums still run on every lane).
+        float part[NV];
 #pragma unroll
         for (int i = 0; i < GH; ++i) {
-          // Head slots past G: q = dO = 0 and Delta = 0, so dS = 0 and
-          // p dO = 0 (the sums still run on every lane).
-          const float s = group_sum<L>(dot_pairs(q2[i], k2));
-          const float dp = group_sum<L>(dot_pairs(do2[i], v2));
-          const float p = valid ? ex2(s * P.scale_log2 - lse2[i]) : 0.f;
-          const float dss = p * (dp - dl[i]) * P.scale;
+          part[2 * i] = dot_pairs(q2[i], k2);
+          part[2 * i + 1] = dot_pairs(do2[i], v2);
+        }
+        const float tot = reduce_scatter<L, NV>(part, l);
+        const float oth = __shfl_xor_sync(0xffffffffu, tot, kPairOff);
+        const float s_me = my_dp ? oth : tot, dp_me = my_dp ? tot : oth;
+        const float p_me = valid ? ex2(s_me * P.scale_log2 - my_lse2) : 0.f;
+        const float dss_me = p_me * (dp_me - my_dl) * P.scale;
+#pragma unroll
+        for (int i = 0; i < GH; ++i) {
+          const float p = __shfl_sync(0xffffffffu, p_me, scatter_lane<L, NV>(2 * i), L);
+          const float dss = __shfl_sync(0xffffffffu, dss_me, scatter_lane<L, NV>(2 * i), L);
           const uint64_t dss2 = f32x2(dss, dss), p2 = f32x2(p, p);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
