@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=[n for n in wl.WORKLOADS if n != "tiny"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--copy-streams", type=int, default=2,
                     help="e2e: copy streams per direction (pieces of <= 64 MB alternate them)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -558,59 +558,69 @@ def run_e2e(a, wb, dev, stream, flops, world):
     all its inputs from pinned host memory and reads all its results back (O,
     lse, dq, dK_j and dV_j of every TTT step, the soft-CE gradient and loss).
 
-    Arranged as a user with host buffers would: copies run on --copy-streams
-    streams per direction in pieces of at most 64 MB, so that several copy
-    engines work in both directions at once; the attention's inputs go first and
-    its results leave while the soft-CE's inputs (the largest) are still coming
-    in (the reverse order measured 143 against 108 ms per long_ttt step, and
-    four streams per direction 156); each TTT step's kernels wait only for that
-    step's inputs, and its results leave while the later steps compute.  A step's
-    copies in wait for the previous step to be done with the device buffers."""
+    Arranged as a user streaming batches from host memory would: copies run on
+    --copy-streams streams per direction in pieces of at most 64 MB, so that
+    several copy engines work in both directions at once; the attention's inputs
+    go first and its results leave while the soft-CE's inputs (the largest) are
+    still coming in (the reverse order measured 143 against 108 ms per long_ttt
+    step); each TTT step's kernels wait only for that step's inputs, and its
+    results leave while the later steps compute.  Consecutive steps use two sets
+    of device buffers, so a step's copies in overlap the previous step's copies
+    out; a step's copies in wait only for the step before the previous one (the
+    last user of its set) to be done."""
     ops, sh = wb.ops, wb.sh
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
     nb = sh.n_blocks
     steps = list(sh.steps)
-    # host inputs (pinned) and their device copies
+    # host inputs (pinned, read by every step)
     hK = [pin(x) for x in wb.Ks]
     hV = [pin(x) for x in wb.Vs]
     hq = {k: pin(wb.qs[k]) for k in steps}
     hd = {k: pin(wb.dOs[k]) for k in steps}
     hz, hp, hg = pin(wb.z0), pin(wb.p), pin(wb.g)
-    dK = [torch.empty_like(x) for x in wb.Ks]
-    dV = [torch.empty_like(x) for x in wb.Vs]
-    dq_ = {k: torch.empty_like(wb.qs[k]) for k in steps}
-    ddo = {k: torch.empty_like(wb.dOs[k]) for k in steps}
-    dz, dp_, dg = torch.empty_like(wb.z0), torch.empty_like(wb.p), torch.empty_like(wb.g)
-    # device results of every step, and pinned host buffers per copy-out stream
-    o_d = {k: torch.empty_like(wb.out) for k in steps}
-    lse_d = {k: torch.empty((sh.B, sh.H, sh.Q_LEN), device=dev, dtype=torch.float32) for k in steps}
-    gq_d = {k: torch.empty(wb.out.shape, device=dev, dtype=torch.float32) for k in steps}
-    gk_d = {k: [torch.empty(wb.Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(k + 1)]
-            for k in steps}
-    gv_d = {k: [torch.empty(wb.Ks[0].shape, device=dev, dtype=torch.float32) for _ in range(k + 1)]
-            for k in steps}
+
+    def device_set():
+        """Device inputs and results of one step."""
+        d = {"K": [torch.empty_like(x) for x in wb.Ks], "V": [torch.empty_like(x) for x in wb.Vs],
+             "q": {k: torch.empty_like(wb.qs[k]) for k in steps},
+             "dO": {k: torch.empty_like(wb.dOs[k]) for k in steps},
+             "z": torch.empty_like(wb.z0), "p": torch.empty_like(wb.p), "g": torch.empty_like(wb.g),
+             "o": {k: torch.empty_like(wb.out) for k in steps},
+             "lse": {k: torch.empty((sh.B, sh.H, sh.Q_LEN), device=dev, dtype=torch.float32)
+                     for k in steps},
+             "gq": {k: torch.empty(wb.out.shape, device=dev, dtype=torch.float32) for k in steps},
+             "gk": {k: [torch.empty(wb.Ks[0].shape, device=dev, dtype=torch.float32)
+                        for _ in range(k + 1)] for k in steps},
+             "gv": {k: [torch.empty(wb.Ks[0].shape, device=dev, dtype=torch.float32)
+                        for _ in range(k + 1)] for k in steps},
+             "loss": torch.empty(1, device=dev, dtype=torch.float32)}
+        return d
+
+    sets = [device_set(), device_set()]
     ws = torch.empty(ops.stt_attn_bwd_workspace_size(sh.B, sh.H, sh.H_kv, sh.D, sh.Q_LEN, max(steps)),
                      device=dev, dtype=torch.uint8)
-    loss_d = torch.empty(1, device=dev, dtype=torch.float32)
     ce_ws = torch.empty(ops.soft_ce_workspace_size(*wb.z0.shape), device=dev, dtype=torch.uint8)
     ns = max(1, a.copy_streams)
+    # pinned host results: per copy-out stream (a stream's copies are ordered),
+    # and the soft-CE gradient per device set (its pieces alternate streams)
     o_h = [torch.empty(wb.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(ns)]
     lse_h = [torch.empty((sh.B, sh.H, sh.Q_LEN), dtype=torch.float32).pin_memory() for _ in range(ns)]
     dq_h = [torch.empty(wb.out.shape, dtype=torch.float32).pin_memory() for _ in range(ns)]
     dkv_h = [[torch.empty(wb.Ks[0].shape, dtype=torch.float32).pin_memory() for _ in range(2 * nb)]
              for _ in range(ns)]
-    z_h = torch.empty(wb.z0.shape, dtype=torch.float32).pin_memory()
-    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    z_h = [torch.empty(wb.z0.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    loss_h = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in hK + hV + list(hq.values()) + list(hd.values()))
     h2d += sum(x.numel() * x.element_size() for x in (hz, hp, hg))
     d2h = 0
     for k in steps:
         d2h += o_h[0].numel() * 2 + lse_h[0].numel() * 4 + dq_h[0].numel() * 4
         d2h += 2 * (k + 1) * dkv_h[0][0].numel() * 4
-    d2h += z_h.numel() * 4 + 4
+    d2h += z_h[0].numel() * 4 + 4
 
     s_in = [torch.cuda.Stream(device=dev) for _ in range(ns)]
     s_out = [torch.cuda.Stream(device=dev) for _ in range(ns)]
+    s_join = torch.cuda.Stream(device=dev)
     piece = 64 << 20
     turn = {"in": 0, "out": 0}
 
@@ -638,77 +648,82 @@ def run_e2e(a, wb, dev, stream, flops, world):
         for e in evs:
             st.wait_event(e)
 
-    def one(prev_done):
-        if prev_done is not None:
+    def one(n, set_free):
+        """Step n on device set n % 2; set_free: the event after which the set's
+        previous step is done with it (None: free)."""
+        d = sets[n % 2]
+        if set_free is not None:
             for st in s_in:
-                st.wait_event(prev_done)
+                st.wait_event(set_free)
         ready = {}
         blocks_in = 0
         for k in steps:
             while blocks_in <= k:   # the blocks this step sees, first time needed
-                copy(dK[blocks_in], hK[blocks_in], "in")
-                copy(dV[blocks_in], hV[blocks_in], "in")
+                copy(d["K"][blocks_in], hK[blocks_in], "in")
+                copy(d["V"][blocks_in], hV[blocks_in], "in")
                 blocks_in += 1
-            copy(dq_[k], hq[k], "in")
-            copy(ddo[k], hd[k], "in")
+            copy(d["q"][k], hq[k], "in")
+            copy(d["dO"][k], hd[k], "in")
             ready[k] = mark(s_in)
-        copy(dz, hz, "in")
-        copy(dp_, hp, "in")
-        copy(dg, hg, "in")
+        copy(d["z"], hz, "in")
+        copy(d["p"], hp, "in")
+        copy(d["g"], hg, "in")
         ce_ready = mark(s_in)
         for i, k in enumerate(steps):
             wait(stream, ready[k])
-            o, l = ops.stt_attn_fwd(dq_[k], dK[: k + 1], dV[: k + 1], wb.T, sh.scale,
-                                    out=o_d[k], lse=lse_d[k], stream=stream)
-            ops.stt_attn_bwd(dq_[k], dK[: k + 1], dV[: k + 1], wb.T, o, ddo[k], l, sh.scale,
-                             dq=gq_d[k], dk_blocks=gk_d[k], dv_blocks=gv_d[k], workspace=ws,
-                             stream=stream)
+            o, l = ops.stt_attn_fwd(d["q"][k], d["K"][: k + 1], d["V"][: k + 1], wb.T, sh.scale,
+                                    out=d["o"][k], lse=d["lse"][k], stream=stream)
+            ops.stt_attn_bwd(d["q"][k], d["K"][: k + 1], d["V"][: k + 1], wb.T, o, d["dO"][k], l,
+                             sh.scale, dq=d["gq"][k], dk_blocks=d["gk"][k], dv_blocks=d["gv"][k],
+                             workspace=ws, stream=stream)
             done = torch.cuda.Event()
             done.record(stream)
             so = s_out[i % ns]   # each copy-out stream reuses only its own host buffers
             so.wait_event(done)
             with torch.cuda.stream(so):
                 hb = i % ns
-                o_h[hb].copy_(o_d[k], non_blocking=True)
-                lse_h[hb].copy_(lse_d[k], non_blocking=True)
-                dq_h[hb].copy_(gq_d[k], non_blocking=True)
+                o_h[hb].copy_(d["o"][k], non_blocking=True)
+                lse_h[hb].copy_(d["lse"][k], non_blocking=True)
+                dq_h[hb].copy_(d["gq"][k], non_blocking=True)
                 for j in range(k + 1):
-                    dkv_h[hb][j].copy_(gk_d[k][j], non_blocking=True)
-                    dkv_h[hb][nb + j].copy_(gv_d[k][j], non_blocking=True)
+                    dkv_h[hb][j].copy_(d["gk"][k][j], non_blocking=True)
+                    dkv_h[hb][nb + j].copy_(d["gv"][k][j], non_blocking=True)
         wait(stream, ce_ready)
-        ops.soft_ce_fwd_bwd_inplace(dz, dp_, dg, loss=loss_d, workspace=ce_ws, want_row_loss=False,
-                                    stream=stream)
+        ops.soft_ce_fwd_bwd_inplace(d["z"], d["p"], d["g"], loss=d["loss"], workspace=ce_ws,
+                                    want_row_loss=False, stream=stream)
         ce_done = torch.cuda.Event()
         ce_done.record(stream)
         for st in s_out:
             st.wait_event(ce_done)
-        copy(z_h, dz, "out")
+        copy(z_h[n % 2], d["z"], "out")
         with torch.cuda.stream(s_out[0]):
-            loss_h.copy_(loss_d, non_blocking=True)
-        # the step ends when every copy out has landed
-        wait(stream, mark(s_out))
+            loss_h[n % 2].copy_(d["loss"], non_blocking=True)
+        # the step ends when every copy out has landed (recorded on a stream of
+        # its own, so the next step's kernels need not wait for these copies)
+        wait(s_join, mark(s_out))
         end = torch.cuda.Event()
-        end.record(stream)
+        end.record(s_join)
         return end
 
-    last = one(None)
+    one(0, None)  # untimed: first touch of every buffer
+    one(1, None)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     e0.record(stream)
-    last = None
-    for _ in range(a.e2e_steps):
-        # the copies in of a step may start only once the previous step's work
-        # on the device buffers is done (the first waits for the start event)
-        last = one(last if last is not None else e0)
+    ends = [e0, e0]
+    for n in range(a.e2e_steps):
+        ends[n % 2] = one(n, ends[n % 2])
+    wait(stream, [ends[(a.e2e_steps - 1) % 2], ends[a.e2e_steps % 2]])
     e1.record(stream)
     torch.cuda.synchronize()
     ms_ = allreduce(e0.elapsed_time(e1), world, dev, "max")
     tot = allreduce(float(flops) * a.e2e_steps, world, dev, "sum")
     return {"value": round(tot / (ms_ * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms_ / a.e2e_steps, 3), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "copy_streams_per_direction": ns}
+            "d2h_bytes_per_step": int(d2h), "copy_streams_per_direction": ns,
+            "device_buffer_sets": 2}
 
 
 # ------------------------------------------------------ oracle on the CPU --
