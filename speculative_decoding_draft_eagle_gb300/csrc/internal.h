@@ -43,6 +43,13 @@ CeVariantPlan soft_ce_variant_plan(const void* z, const void* p, const float* g,
 cudaError_t soft_ce_variant_launch(const CeVariantPlan& plan, uint32_t flags, void* z,
                                    const void* p, const float* g, int64_t N, int64_t V,
                                    float* row_loss, float* loss, float* wl, cudaStream_t s);
+// The variants on the persistent cluster kernel (rows 16-byte aligned, V a
+// multiple of 8, slices within its registers' reach); cudaErrorNotSupported
+// when a call does not fit it, before anything is launched.
+cudaError_t soft_ce_variant_persistent_launch(uint32_t flags, void* z, const void* p,
+                                              const float* g, int64_t N, int64_t V,
+                                              float* row_loss, float* loss, float* wl,
+                                              cudaStream_t s);
 
 // ------------------------------------------------------- LM head + soft-CE --
 size_t lm_head_ce_workspace(int64_t N, int64_t V);

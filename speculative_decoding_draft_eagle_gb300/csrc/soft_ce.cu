@@ -324,9 +324,44 @@ struct CeRowRegs {
   float m;        // the warp's max m_w
 };
 
-template <bool SPLIT>
+// Four consecutive elements (group i) of a row slice in shared memory as
+// fp32: float4, or four bf16 (8 bytes) widened.
+template <bool BF16>
+__device__ __forceinline__ float4 lds_group(const unsigned char* base, int i) {
+  if constexpr (BF16) {
+    const uint2 u = reinterpret_cast<const uint2*>(base)[i];
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  } else {
+    return reinterpret_cast<const float4*>(base)[i];
+  }
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// Four gradient values (group i of a row slice starting at `row`) to global
+// memory with streaming stores: fp32, or bf16 rounded to nearest even.
+template <bool BF16>
+__device__ __forceinline__ void stg_group(void* row, int i, float4 v) {
+  if constexpr (BF16) {
+    asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(static_cast<uint2*>(row) + i),
+                 "r"(bf16x2_rn(v.x, v.y)), "r"(bf16x2_rn(v.z, v.w))
+                 : "memory");
+  } else {
+    st_global_cs_f4(static_cast<float*>(row) + 4 * i, v);
+  }
+}
+
+// SPLIT: the split layout of large fp32 slices.  BF16: z and p are bf16 (the
+// gradient is written back in bf16).  GEL: g is per element ([N, V] fp32): the
+// row's sums take p g in place of p, and no row is masked.
+template <bool SPLIT, bool BF16 = false, bool GEL = false>
 __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const CePParams P) {
+  static_assert(!SPLIT || (!BF16 && !GEL), "the split layout is fp32 with a per-row g");
   constexpr int VEC = SPLIT ? kPVecSplit : kPVec;
+  constexpr int ESZ = BF16 ? 2 : 4;                      // bytes per z / p element
+  constexpr int PER = 2 * ESZ + (GEL ? 4 : 0);           // buffer bytes per element (unsplit)
   using Row = CeRowRegs<VEC, !SPLIT>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ uint64_t full[kPMaxBufs];
@@ -344,13 +379,19 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
   const long long rem = P.V - begin;
   const int len = rem <= 0 ? 0 : (rem < P.slice ? (int)rem : P.slice);
   const int n4 = len >> 2;
-  const int nb = SPLIT ? 2 : P.nb;  // z (and, unsplit, p) buffers
-  float* const sbase = reinterpret_cast<float*>(smem_raw);
-  // Buffer b of z (and of p when unsplit); p buffer c of the split layout.
-  auto zbuf = [&](int b) { return sbase + (size_t)b * (SPLIT ? 1 : 2) * P.slice; };
-  auto pbuf = [&](int b, int c) {
-    return SPLIT ? sbase + (size_t)(2 + c) * P.slice : sbase + (size_t)b * 2 * P.slice + P.slice;
+  const int nb = SPLIT ? 2 : P.nb;  // z (and, unsplit, p and g) buffers
+  // Buffer b of z (and, unsplit, of p and of a per-element g); p buffer c of
+  // the split layout.
+  auto zbuf = [&](int b) {
+    return smem_raw + (size_t)b * (SPLIT ? 4 : PER) * P.slice;
   };
+  auto pbuf = [&](int b, int c) {
+    return SPLIT ? smem_raw + (size_t)(2 + c) * 4 * P.slice
+                 : smem_raw + (size_t)b * PER * P.slice + (size_t)ESZ * P.slice;
+  };
+  auto gbuf = [&](int b) { return smem_raw + (size_t)b * PER * P.slice + (size_t)2 * ESZ * P.slice; };
+  // The rows' per-row weight (1 with a per-element g: such rows are never masked).
+  auto row_g = [&](long long r) -> float { return GEL ? 1.0f : __ldg(P.g + r); };
 
   if (tid == 0) {
     for (int b = 0; b < nb; ++b) {
@@ -375,33 +416,36 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     // Producer: the slices of the cluster's rows with g != 0, in order.
     if (lane == 0 && len > 0) {
       int j = 0;
-      float gr = cid < P.N ? __ldg(P.g + cid) : 0.0f;
+      float gr = cid < P.N ? row_g(cid) : 0.0f;
       for (long long r = cid; r < P.N; r += ncl) {
         const float gcur = gr;
-        if (r + ncl < P.N) gr = __ldg(P.g + r + ncl);
+        if (r + ncl < P.N) gr = row_g(r + ncl);
         if (gcur == 0.0f) continue;
         const int b = j % nb;
         if (j >= nb) mbar_wait(&empty[b], (uint32_t)(j / nb - 1) & 1u, STT_DEVERR_CE_WAIT);
-        float* zs = zbuf(b);
-        const float* zsrc = P.z + r * P.V + begin;
-        const float* psrc = P.p + r * P.V + begin;
+        unsigned char* zs = zbuf(b);
+        const unsigned char* zsrc = reinterpret_cast<const unsigned char*>(P.z) + (r * P.V + begin) * ESZ;
+        const unsigned char* psrc = reinterpret_cast<const unsigned char*>(P.p) + (r * P.V + begin) * ESZ;
         if (SPLIT) {
           mbar_arrive_expect_tx(&full[b], 4u * (uint32_t)len);
           for (int c = 0; c < len; c += kChunk)
-            bulk_load(zs + c, zsrc + c, (uint32_t)min(kChunk, len - c) * 4u, &full[b]);
+            bulk_load(zs + 4 * c, zsrc + 4 * c, (uint32_t)min(kChunk, len - c) * 4u, &full[b]);
           const int pc = j % 3;
           if (j >= 3) mbar_wait(&pempty[pc], (uint32_t)(j / 3 - 1) & 1u, STT_DEVERR_CE_WAIT);
-          float* ps = pbuf(b, pc);
+          unsigned char* ps = pbuf(b, pc);
           mbar_arrive_expect_tx(&pfull[pc], 4u * (uint32_t)len);
           for (int c = 0; c < len; c += kChunk)
-            bulk_load(ps + c, psrc + c, (uint32_t)min(kChunk, len - c) * 4u, &pfull[pc]);
+            bulk_load(ps + 4 * c, psrc + 4 * c, (uint32_t)min(kChunk, len - c) * 4u, &pfull[pc]);
         } else {
-          float* ps = pbuf(b, 0);
-          mbar_arrive_expect_tx(&full[b], 8u * (uint32_t)len);
+          unsigned char* ps = pbuf(b, 0);
+          unsigned char* gs = gbuf(b);
+          const float* gsrc = P.g + r * P.V + begin;
+          mbar_arrive_expect_tx(&full[b], (uint32_t)PER * (uint32_t)len);
           for (int c = 0; c < len; c += kChunk) {
-            const uint32_t bytes = (uint32_t)min(kChunk, len - c) * 4u;
-            bulk_load(zs + c, zsrc + c, bytes, &full[b]);
-            bulk_load(ps + c, psrc + c, bytes, &full[b]);
+            const uint32_t n = (uint32_t)min(kChunk, len - c);
+            bulk_load(zs + (size_t)ESZ * c, zsrc + (size_t)ESZ * c, n * ESZ, &full[b]);
+            bulk_load(ps + (size_t)ESZ * c, psrc + (size_t)ESZ * c, n * ESZ, &full[b]);
+            if (GEL) bulk_load(gs + (size_t)4 * c, gsrc + c, n * 4u, &full[b]);
           }
         }
         ++j;
@@ -412,26 +456,26 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     // Consumers.
     Row ra, rb;
     long long row = cid;
-    float g_row = cid < P.N ? __ldg(P.g + cid) : 0.0f;
+    float g_row = cid < P.N ? row_g(cid) : 0.0f;
     int v = 0;  // valid rows reduced so far
 
     // Moves `row` to the cluster's next row with g != 0, writing zeros (and
     // zero losses) for the masked rows passed on the way.  False at the end.
     auto next_valid = [&]() -> bool {
       while (row < P.N && g_row == 0.0f) {
-        float* zrow = P.z + row * P.V + begin;
+        void* zrow = reinterpret_cast<unsigned char*>(P.z) + (row * P.V + begin) * ESZ;
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
-          if (i < n4) st_global_cs_f4(zrow + 4 * i, zero);
+          if (i < n4) stg_group<BF16>(zrow, i, zero);
         }
         if (rank == 0 && tid == 0) {
           if (P.row_loss) P.row_loss[row] = 0.0f;
           P.wl[row] = 0.0f;
         }
         row += ncl;
-        g_row = row < P.N ? __ldg(P.g + row) : 0.0f;
+        g_row = row < P.N ? row_g(row) : 0.0f;
       }
       return row < P.N;
     };
@@ -439,12 +483,13 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
     // reduce(v) of the current row into `cur`, then push the warp partial.
     auto reduce = [&](Row& cur) {
       const int b = v % nb;
-      const float4* zs4 = reinterpret_cast<const float4*>(zbuf(b));
-      const float4* ps4 = reinterpret_cast<const float4*>(pbuf(b, v % 3));
+      const unsigned char* zs = zbuf(b);
+      const unsigned char* ps = pbuf(b, v % 3);
+      const float4* gs4 = reinterpret_cast<const float4*>(gbuf(b));
       cur.row = row;
       cur.g = g_row;
       row += ncl;
-      g_row = row < P.N ? __ldg(P.g + row) : 0.0f;
+      g_row = row < P.N ? row_g(row) : 0.0f;
       float m = -INFINITY;
       if (len > 0) {
         mbar_wait(&full[b], (uint32_t)(v / nb) & 1u, STT_DEVERR_CE_WAIT);
@@ -453,8 +498,16 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
         for (int k = 0; k < VEC; ++k) {
           const int i = tid + k * kPConsumers;
           if (i < n4) {
-            cur.e[k] = zs4[i];
-            if constexpr (!SPLIT) cur.p[k] = ps4[i];
+            cur.e[k] = lds_group<BF16>(zs, i);
+            if constexpr (!SPLIT) {
+              cur.p[k] = lds_group<BF16>(ps, i);
+              if constexpr (GEL) {
+                // p g per element stands in for p from here on
+                const float4 gv = gs4[i];
+                cur.p[k] = make_float4(cur.p[k].x * gv.x, cur.p[k].y * gv.y, cur.p[k].z * gv.z,
+                                       cur.p[k].w * gv.w);
+              }
+            }
           }
         }
         __syncwarp();
@@ -478,7 +531,7 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
             const float4 zv = cur.e[k];
             float4 pv;
             if constexpr (SPLIT)
-              pv = ps4[i];
+              pv = lds_group<false>(ps, i);
             else
               pv = cur.p[k];
             float4 e;
@@ -532,15 +585,15 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
       const float g = prv.g;
       // exp(z - lse) g Sp = e exp(m_w - lse) g Sp; m_w <= lse, so this cannot overflow.
       const float scale = (prv.m == -INFINITY) ? 0.f : ex2((prv.m - lse) * kLog2e) * (g * Sp);
-      float* zrow = P.z + prv.row * P.V + begin;
-      const float4* ps4 = reinterpret_cast<const float4*>(pbuf(0, u % 3));
+      void* zrow = reinterpret_cast<unsigned char*>(P.z) + (prv.row * P.V + begin) * ESZ;
+      const unsigned char* ps = pbuf(0, u % 3);
 #pragma unroll
       for (int k = 0; k < VEC; ++k) {
         const int i = tid + k * kPConsumers;
         if (i < n4) {
           float4 pv;
           if constexpr (SPLIT)
-            pv = ps4[i];
+            pv = lds_group<false>(ps, i);
           else
             pv = prv.p[k];
           float4 o;
@@ -548,7 +601,7 @@ __global__ void __launch_bounds__(kPThreads, 1) soft_ce_persistent_kernel(const 
           o.y = fmaf(prv.e[k].y, scale, -pv.y * g);
           o.z = fmaf(prv.e[k].z, scale, -pv.z * g);
           o.w = fmaf(prv.e[k].w, scale, -pv.w * g);
-          st_global_cs_f4(zrow + 4 * i, o);
+          stg_group<BF16>(zrow, i, o);
         }
       }
       if (SPLIT && len > 0) {
@@ -684,10 +737,10 @@ CePlan soft_ce_plan(const float* z, const float* p, int64_t N, int64_t V) {
 
 namespace {
 
-// Co-resident clusters of soft_ce_persistent_kernel<SPLIT> for (C, smem) on
-// the current device; 0 if the query fails.  Cached per device (and SPLIT) for
-// the last configuration.
-template <bool SPLIT>
+// Co-resident clusters of soft_ce_persistent_kernel<SPLIT, BF16, GEL> for
+// (C, smem) on the current device; 0 if the query fails.  Cached per device
+// (and instantiation) for the last configuration.
+template <bool SPLIT, bool BF16 = false, bool GEL = false>
 int persistent_clusters(int C, int smem) {
   static std::mutex mu;
   static int cache_dev[64], cache_C[64], cache_smem[64], cache_n[64];
@@ -700,12 +753,11 @@ int persistent_clusters(int C, int smem) {
     init = true;
   }
   if (cache_dev[dev] == dev && cache_C[dev] == C && cache_smem[dev] == smem) return cache_n[dev];
-  if (cudaFuncSetAttribute(soft_ce_persistent_kernel<SPLIT>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  auto kern = soft_ce_persistent_kernel<SPLIT, BF16, GEL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
-  if (C > 8 && cudaFuncSetAttribute(soft_ce_persistent_kernel<SPLIT>,
-                                    cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                    1) != cudaSuccess)
+  if (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                   cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)C, 1, 1);
@@ -719,7 +771,7 @@ int persistent_clusters(int C, int smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, soft_ce_persistent_kernel<SPLIT>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -816,6 +868,72 @@ cudaError_t soft_ce_loss_sum_launch(const float* wl, int64_t N, float* loss, cud
   lc.attrs = la;
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, soft_ce_loss_sum, wl, (long long)N, loss);
+}
+
+namespace {
+
+template <bool BF16, bool GEL>
+cudaError_t variant_persistent(void* z, const void* p, const float* g, int64_t N, int64_t V,
+                               float* row_loss, float* loss, float* wl, cudaStream_t s) {
+  constexpr int per = 2 * (BF16 ? 2 : 4) + (GEL ? 4 : 0);  // shared bytes per element
+  // Slices of about kPSliceTarget elements (at most kPSliceMax, the registers'
+  // reach), multiples of 8 so that every bf16 slice starts 16-byte aligned.
+  long long C = (V + kPSliceTarget - 1) / kPSliceTarget;
+  const long long Cmin = (V + kPSliceMax - 1) / kPSliceMax;
+  if (C < Cmin) C = Cmin;
+  if (C < 1) C = 1;
+  if (C > kMaxCluster) return cudaErrorNotSupported;
+  long long sl = ((V + C - 1) / C + 7) / 8 * 8;
+  while (C > 1 && (C - 1) * sl >= V) {
+    --C;
+    sl = ((V + C - 1) / C + 7) / 8 * 8;
+  }
+  if (sl > kPSliceMax) return cudaErrorNotSupported;
+  long long nb = kPSmemBudget / (per * sl);
+  if (nb > kPMaxBufs) nb = kPMaxBufs;
+  if (nb < kPMinBufs) return cudaErrorNotSupported;
+  const int smem = (int)(nb * per * sl);
+  const int ncl = persistent_clusters<false, BF16, GEL>((int)C, smem);
+  if (ncl <= 0) return cudaErrorNotSupported;
+  const long long n_clusters = ncl < N ? ncl : N;
+  CePParams P{static_cast<float*>(z), static_cast<const float*>(p), g, row_loss, wl,
+              (long long)N, (long long)V, (int)C, (int)sl, (int)nb};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_clusters * C), 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_before(s, STT_KERNEL_SOFT_CE_VARIANT);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, soft_ce_persistent_kernel<false, BF16, GEL>, P);
+  if (e == cudaSuccess) e = soft_ce_loss_sum_launch(wl, N, loss, s);
+  prof_after(s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t soft_ce_variant_persistent_launch(uint32_t flags, void* z, const void* p,
+                                              const float* g, int64_t N, int64_t V,
+                                              float* row_loss, float* loss, float* wl,
+                                              cudaStream_t s) {
+  const bool bf16 = (flags & kCeBf16) != 0, gel = (flags & kCeGPerElement) != 0;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(p) |
+                      (gel ? reinterpret_cast<uintptr_t>(g) : 0);
+  // bf16 rows with a per-row g stay on the one-row-per-cluster kernel: at
+  // 6 bytes an element the persistent kernel's per-row exchange and arithmetic,
+  // not its bytes, set its pace (2.8 against 4.2 TB/s at V = 32000).
+  if (N <= 0 || V % 8 != 0 || (a & 15u) != 0 || (bf16 && !gel)) return cudaErrorNotSupported;
+  if (bf16) return variant_persistent<true, true>(z, p, g, N, V, row_loss, loss, wl, s);
+  return gel ? variant_persistent<false, true>(z, p, g, N, V, row_loss, loss, wl, s)
+             : variant_persistent<false, false>(z, p, g, N, V, row_loss, loss, wl, s);
 }
 
 STT_DEFINE_ERROR_ACCESSOR(soft_ce_error_word)

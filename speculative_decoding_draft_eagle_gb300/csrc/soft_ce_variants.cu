@@ -346,6 +346,10 @@ cudaError_t soft_ce_variant_launch(const CeVariantPlan& plan, uint32_t flags, vo
                                    const void* p, const float* g, int64_t N, int64_t V,
                                    float* row_loss, float* loss, float* wl, cudaStream_t s) {
   const bool bf16 = (flags & kCeBf16) != 0, gel = (flags & kCeGPerElement) != 0;
+  // Aligned rows that fit the persistent cluster kernel take it; the rest the
+  // one-row-per-cluster kernel below.
+  const cudaError_t ep = soft_ce_variant_persistent_launch(flags, z, p, g, N, V, row_loss, loss, wl, s);
+  if (ep != cudaErrorNotSupported) return ep;
   if (N > 0) {
     if (N * (long long)plan.C > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CeVParams P{z, p, g, row_loss, wl, (long long)N, (long long)V, plan.C, plan.slice, plan.chunk};
