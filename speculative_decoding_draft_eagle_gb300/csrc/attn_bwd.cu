@@ -8,11 +8,13 @@
 //     dq = scale dS Kc,  dKc = scale dS^T q,  dVc = P^T dO.
 //
 // Two kernels, in stream order:
-//   1. prep (CUDA cores, one warp per (b, KV head, row q)): Delta for every
-//      query head of the group; the whole backward of the diagonal suffix keys
-//      (q < T, blocks j = 1..k: one key per query, so dK_j / dV_j row q is owned
-//      by this warp and written directly); dq initialised with the suffix part;
-//      dK_0 / dV_0 zeroed for the causal kernel's accumulation.
+//   1. prep (CUDA cores fed by bulk copies, one CTA per SM walking units of
+//      rows of one (b, KV head); per (b, KV head, row q) a lane group): Delta
+//      for every query head of the group; the whole backward of the diagonal
+//      suffix keys (q < T, blocks j = 1..k: one key per query, so dK_j / dV_j
+//      row q is owned by one lane group and written directly); dq initialised
+//      with the suffix part; dK_0 / dV_0 zeroed for the causal kernel's
+//      accumulation.
 //   2. causal (tcgen05, one CTA per 128-row key tile of a subgroup of the
 //      query heads of one KV group, looping over the heads' query tiles that
 //      see it, head after head): S^T = K Q^T and dP^T = V dO^T in
