@@ -21,6 +21,7 @@ workloads (fewer steps).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import csv
 import hashlib
 import io
@@ -66,7 +67,7 @@ def parse():
     ap.add_argument("--no-other-workloads", action="store_true")
     ap.add_argument("--other-steps", type=int, default=5)
     ap.add_argument("--no-extras", action="store_true")
-    ap.add_argument("--profile", choices=["attn", "lm_head", "verify"], default=None,
+    ap.add_argument("--profile", choices=["attn", "lm_head", "verify", "soft_ce"], default=None,
                     help="small profiling case (a few GB): 2 calls of one row and exit")
     ap.add_argument("--profile-step", type=int, default=None,
                     help="with --profile attn: the TTT step (default: the workload's last)")
@@ -853,7 +854,8 @@ def run_reference(a):
 def run_profile_case(a):
     """Two calls of one row on bounded memory, for ncu captures: the attention
     forward + backward at one TTT step of the workload (inputs of that step
-    only), the fused LM head, or the verifier.  Prints nothing measured."""
+    only), the workload's soft-CE on 1024 of its rows, the fused LM head, or the
+    verifier.  Prints nothing measured."""
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     from speculative_decoding_draft_eagle_gb300 import build, ops
@@ -869,6 +871,13 @@ def run_profile_case(a):
         for _ in range(2):
             out, lse = ops.stt_attn_fwd(q, Ks, Vs, T, sh.scale)
             ops.stt_attn_bwd(q, Ks, Vs, T, out, dO, lse, sh.scale)
+    elif a.profile == "soft_ce":
+        # the workload's soft-CE rows, 1024 of them (its vocabulary, so the same
+        # slice layout as the full call; about 1.2 GB of z and p)
+        sc = wl.WORKLOADS[a.workload].soft_ce
+        z0, p, g = wl.soft_ce_inputs(dataclasses.replace(sc, N=1024, mask_beyond_T=False), dev, 1007)
+        for _ in range(2):
+            ops.soft_ce_fwd_bwd_inplace(z0.clone(), p, g)
     elif a.profile == "lm_head":
         h, W, p, g = wl.lm_head_inputs(wl.LM_HEAD, dev, 1002)
         for _ in range(2):
